@@ -1,0 +1,126 @@
+"""fp64 CPU oracle for grouped-query attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+legs of ``bench.py`` import this package.  The product library never does, and
+this package imports nothing from it.
+
+The arithmetic lives in ``gqa_oracle.c`` (plain C, OpenMP over output rows);
+this module only compiles it with gcc and marshals numpy arrays through ctypes.
+Every function follows the steps stated in that file's header:
+
+* widen bf16 to fp64 exactly;
+* expand K/V per group (query head h reads KV head h // (Hq // Hkv)), the
+  ``repeat_interleave`` of "手把手教你用PyTorch实现GQA" section 1.3 and the
+  ``repeat_kv`` of the GQA paper notes ("QA 相关", inference);
+* scores = q.k * scale, causal removal of future keys, softmax, @ V
+  (the Huawei Cloud post "多头注意力机制的代码实现（MQA和GQA）", section 5).
+
+Inputs are numpy arrays: ``np.uint16`` holding bf16 bit patterns, or
+``np.float64``.  Outputs are ``np.float64``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gqa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+EMPTY_CONTEXT = 3
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (-O2, OpenMP) if missing or stale."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        p = ctypes.c_void_p
+        i = ctypes.c_int
+        lib.gqa_oracle_decode.argtypes = [p, p, p, i, p, i, i, i, i, i, ctypes.c_double, p, i, p]
+        lib.gqa_oracle_decode.restype = i
+        lib.gqa_oracle_prefill.argtypes = [p, p, p, i, i, i, i, i, i, i, ctypes.c_double, p, i, p]
+        lib.gqa_oracle_prefill.restype = i
+        lib.gqa_oracle_num_threads.restype = i
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle runs on (OMP_NUM_THREADS, else all cores)."""
+    return int(_load().gqa_oracle_num_threads())
+
+
+def _prep(*arrays):
+    dtypes = {a.dtype for a in arrays}
+    if len(dtypes) != 1 or next(iter(dtypes)) not in (np.dtype(np.uint16), np.dtype(np.float64)):
+        raise TypeError("oracle inputs must all be uint16 (bf16 bits) or all float64")
+    etype = 0 if arrays[0].dtype == np.uint16 else 1
+    return [np.ascontiguousarray(a) for a in arrays], etype
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def decode(q, k_cache, v_cache, seqlens, scale=None, rows=None, check=True):
+    """Decode attention of one new query token per (b, h).
+
+    q [B, Hq, D]; k_cache, v_cache [B, Hkv, Lmax, D]; seqlens [B] (int).
+    rows: optional int array [n, 2] of (b, h) to evaluate (default: all, b-major).
+    Returns fp64 [B, Hq, D] (rows=None) or [n, D].
+    """
+    (q, k_cache, v_cache), etype = _prep(q, k_cache, v_cache)
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or k_cache.shape[0] != B:
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32).reshape(B))
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+    n = B * Hq if r is None else r.shape[0]
+    out = np.empty((n, D), dtype=np.float64)
+    rc = _load().gqa_oracle_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), etype, _ptr(sl),
+                                   B, Hq, Hkv, D, Lmax, float(scale), _ptr(r), n, _ptr(out))
+    if check and rc not in (0,):
+        raise ValueError(f"oracle decode returned {rc}")
+    return out.reshape(B, Hq, D) if r is None else out
+
+
+def prefill(q, k, v, causal=True, scale=None, rows=None, check=True):
+    """Prefill attention.
+
+    q [B, Hq, L, D]; k, v [B, Hkv, L, D].  rows: optional int array [n, 3] of
+    (b, h, i).  Returns fp64 [B, Hq, L, D] (rows=None) or [n, D].
+    """
+    (q, k, v), etype = _prep(q, k, v)
+    B, Hq, L, D = q.shape
+    _, Hkv, L2, D2 = k.shape
+    if L2 != L or D2 != D or v.shape != k.shape or k.shape[0] != B:
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    n = B * Hq * L if r is None else r.shape[0]
+    out = np.empty((n, D), dtype=np.float64)
+    rc = _load().gqa_oracle_prefill(_ptr(q), _ptr(k), _ptr(v), etype, B, L, Hq, Hkv, D,
+                                    int(bool(causal)), float(scale), _ptr(r), n, _ptr(out))
+    if check and rc != 0:
+        raise ValueError(f"oracle prefill returned {rc}")
+    return out.reshape(B, Hq, L, D) if r is None else out

@@ -1,0 +1,219 @@
+/*
+ * gqa_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, fp64 CPU statement of grouped-query attention.  Only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg load this file's
+ * library; the product path (libgqa.so and its Python binding) never does, and
+ * this file shares no code, header or constant with it.
+ *
+ * What it computes, step by step, in the order the pages give it:
+ *
+ *   (1) every input element is widened to fp64 exactly (a bf16 value is the top
+ *       16 bits of an fp32, so the widening is lossless);
+ *   (2) K and V are expanded per group exactly as `repeat_interleave(n_rep,
+ *       dim=1)` does: query head h reads KV head h / n_rep with n_rep = Hq/Hkv
+ *       ("手把手教你用PyTorch实现GQA", section 1.3, class GQA; the GQA paper
+ *       notes on 51969.com, "QA 相关" -> inference, `repeat_kv`; the Huawei Cloud
+ *       post "多头注意力机制的代码实现（MQA和GQA）", section 5,
+ *       `group_index = head_index // n_head_per_group`);
+ *   (3) scores  x_t = <q, k_t>            (Huawei Cloud post, section 5: Q @ K^T)
+ *   (4) scaled  x_t = x_t * scale         (same code: divide by head_size**0.5;
+ *       the caller passes scale = 1/sqrt(D) unless it wants another one)
+ *   (5) causal mask: a key strictly after the query position is removed
+ *       (same code: triu(ones, diagonal=1) -> -inf, applied as the code
+ *       intends; the printed `masked_fill` result is discarded, which is read
+ *       as a slip of the page);
+ *   (6) p_t = exp(x_t - max) / sum exp(x_t - max)   (softmax over keys; the
+ *       max shift changes nothing mathematically and only keeps exp in range)
+ *   (7) out = sum_t p_t v_t                (attention @ V)
+ *
+ * Decode: one query token per (b, h) attends to the first seqlens[b] rows of
+ * the [B, Hkv, Lmax, D] cache (no mask inside the cache).  Prefill: q, k, v of
+ * one length L; row i sees keys t <= i when causal, all L keys otherwise.
+ *
+ * Element types: 0 = bf16 bit patterns (uint16), 1 = fp64.  Outputs are fp64.
+ * Rows to evaluate are given as an index list so that sampled rows of a
+ * full-size workload can be checked one by one.
+ *
+ * Return codes: 0 ok, 1 bad argument, 2 out of memory, 3 empty context (no
+ * visible key: the softmax of nothing is undefined; the row is written as
+ * zeros and 3 is returned after the other rows were computed).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double elem(const void *base, size_t i, int type)
+{
+    if (type == 1) return ((const double *)base)[i];
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f; /* step (1): exact */
+}
+
+/* One query row against `nk` visible keys of one (b, h).
+ * kx, vx: the expanded K/V rows of this query head, [nk, D] fp64.
+ * Writes out[D].  Returns 0, or 3 if nk == 0. */
+static int attend_row(const double *qrow, const double *kx, const double *vx, int nk, int D,
+                      double scale, double *x, double *out)
+{
+    if (nk <= 0) {
+        for (int d = 0; d < D; ++d) out[d] = 0.0;
+        return 3;
+    }
+    /* (3) + (4) */
+    for (int t = 0; t < nk; ++t) {
+        double s = 0.0;
+        for (int d = 0; d < D; ++d) s += qrow[d] * kx[(size_t)t * D + d];
+        x[t] = s * scale;
+    }
+    /* (6) */
+    double mx = -INFINITY;
+    for (int t = 0; t < nk; ++t)
+        if (x[t] > mx) mx = x[t];
+    double den = 0.0;
+    for (int t = 0; t < nk; ++t) {
+        x[t] = exp(x[t] - mx);
+        den += x[t];
+    }
+    for (int t = 0; t < nk; ++t) x[t] /= den;
+    /* (7) */
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (int t = 0; t < nk; ++t)
+        for (int d = 0; d < D; ++d) out[d] += x[t] * vx[(size_t)t * D + d];
+    return 0;
+}
+
+/* Step (2) for one query head: gather the rows [0, n) of KV head h / n_rep of
+ * batch b into dense fp64 buffers, i.e. the slice of repeat_interleave(K)
+ * that query head h sees. */
+static void expand_head(const void *k, const void *v, int type, int b, int h, int n_rep,
+                        int Hkv, int Lcap, int D, int n, double *kx, double *vx)
+{
+    int j = h / n_rep;
+    size_t base = (((size_t)b * Hkv + j) * Lcap) * D;
+    for (size_t i = 0; i < (size_t)n * D; ++i) {
+        kx[i] = elem(k, base + i, type);
+        vx[i] = elem(v, base + i, type);
+    }
+}
+
+/* Decode.
+ *   q        [B, Hq, D]            out rows of the evaluated (b, h): [nrows, D]
+ *   k, v     [B, Hkv, Lmax, D]     seqlens [B] (keys visible to batch b)
+ *   rows     (b, h) int pairs, nrows of them; rows == NULL means all B*Hq in
+ *            order b-major, h-minor. */
+int gqa_oracle_decode(const void *q, const void *k, const void *v, int type,
+                      const int32_t *seqlens, int B, int Hq, int Hkv, int D, int Lmax,
+                      double scale, const int32_t *rows, int nrows, double *out)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax <= 0 || Hq % Hkv != 0) return 1;
+    if (type != 0 && type != 1) return 1;
+    if (rows == NULL) nrows = B * Hq;
+    for (int b = 0; b < B; ++b)
+        if (seqlens[b] > Lmax) return 1;
+    int n_rep = Hq / Hkv;
+    int rc_all = 0;
+#pragma omp parallel
+    {
+        double *kx = malloc(sizeof(double) * (size_t)Lmax * D);
+        double *vx = malloc(sizeof(double) * (size_t)Lmax * D);
+        double *x = malloc(sizeof(double) * (size_t)Lmax);
+        double *qrow = malloc(sizeof(double) * (size_t)D);
+        int oom = !(kx && vx && x && qrow);
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < nrows; ++r) {
+            int rc;
+            if (oom) {
+                rc = 2;
+            } else {
+                int b = rows ? rows[2 * r] : r / Hq;
+                int h = rows ? rows[2 * r + 1] : r % Hq;
+                if (b < 0 || b >= B || h < 0 || h >= Hq) {
+                    rc = 1;
+                } else {
+                    int n = seqlens[b] > 0 ? seqlens[b] : 0;
+                    for (int d = 0; d < D; ++d) qrow[d] = elem(q, ((size_t)b * Hq + h) * D + d, type);
+                    expand_head(k, v, type, b, h, n_rep, Hkv, Lmax, D, n, kx, vx);
+                    rc = attend_row(qrow, kx, vx, n, D, scale, x, out + (size_t)r * D);
+                }
+            }
+            if (rc) {
+#pragma omp critical
+                if (rc_all == 0 || rc < rc_all) rc_all = rc;
+            }
+        }
+        free(kx); free(vx); free(x); free(qrow);
+    }
+    return rc_all;
+}
+
+/* Prefill.
+ *   q, out   [B, Hq, L, D]         k, v [B, Hkv, L, D]
+ *   rows     (b, h, i) int triples, nrows of them; rows == NULL means every
+ *            (b, h, i) in row-major order.
+ *   causal   1: row i sees keys t <= i (square mask, query i at position i);
+ *            0: every row sees all L keys. */
+int gqa_oracle_prefill(const void *q, const void *k, const void *v, int type,
+                       int B, int L, int Hq, int Hkv, int D, int causal, double scale,
+                       const int32_t *rows, int nrows, double *out)
+{
+    if (B <= 0 || L <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return 1;
+    if ((causal != 0 && causal != 1) || (type != 0 && type != 1)) return 1;
+    if (rows == NULL) nrows = B * Hq * L;
+    int n_rep = Hq / Hkv;
+    int rc_all = 0;
+#pragma omp parallel
+    {
+        double *kx = malloc(sizeof(double) * (size_t)L * D);
+        double *vx = malloc(sizeof(double) * (size_t)L * D);
+        double *x = malloc(sizeof(double) * (size_t)L);
+        double *qrow = malloc(sizeof(double) * (size_t)D);
+        int oom = !(kx && vx && x && qrow);
+        int cur_b = -1, cur_h = -1;
+#pragma omp for schedule(dynamic, 16)
+        for (int r = 0; r < nrows; ++r) {
+            int rc;
+            if (oom) {
+                rc = 2;
+            } else {
+                int b = rows ? rows[3 * r] : r / (Hq * L);
+                int h = rows ? rows[3 * r + 1] : (r / L) % Hq;
+                int i = rows ? rows[3 * r + 2] : r % L;
+                if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= L) {
+                    rc = 1;
+                } else {
+                    if (b != cur_b || h != cur_h) {
+                        expand_head(k, v, type, b, h, n_rep, Hkv, L, D, L, kx, vx);
+                        cur_b = b;
+                        cur_h = h;
+                    }
+                    int n = causal ? i + 1 : L; /* (5) */
+                    for (int d = 0; d < D; ++d)
+                        qrow[d] = elem(q, (((size_t)b * Hq + h) * L + i) * D + d, type);
+                    rc = attend_row(qrow, kx, vx, n, D, scale, x, out + (size_t)r * D);
+                }
+            }
+            if (rc) {
+#pragma omp critical
+                if (rc_all == 0 || rc < rc_all) rc_all = rc;
+            }
+        }
+        free(kx); free(vx); free(x); free(qrow);
+    }
+    return rc_all;
+}
+
+int gqa_oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

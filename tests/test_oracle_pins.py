@@ -1,0 +1,300 @@
+"""Pins of the fp64 oracle to facts that do not come from the oracle itself.
+
+Each test names the passage it follows.  The pins are chosen so that a
+plausible slip in the oracle fails at least one of them:
+
+* a wrong head -> KV-head map (h mod Hkv instead of h div G): group-constant V,
+  library SDPA with enable_gqa, materialised repeat_interleave;
+* a dropped or wrong scale, a transposed operand: library SDPA, the two-key
+  logistic closed form;
+* a missing normalisation: constant V;
+* a causal diagonal off by one / a mask that leaks the future: row 0 = v_0,
+  the i/2 staircase, future-perturbation invariance;
+* reading cache rows past seqlens[b]: the NaN-tail test;
+* a lossy bf16 widening: exact bit patterns.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from grouped_query_attention_09_b300 import workloads as W
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+
+def bf16(a):
+    """Rounds an fp64 array to bf16 (RNE) and returns (bits uint16, exact fp64 values)."""
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return W.bf16_bits(t), t.double().numpy()
+
+
+def rnd(shape, seed, mult=1.0):
+    g = np.random.default_rng(seed)
+    return g.standard_normal(shape) * mult
+
+
+def sdpa(q, k, v, causal=False, scale=None):
+    """torch fp64 scaled_dot_product_attention with grouped K/V (a library routine)."""
+    return F.scaled_dot_product_attention(torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v),
+                                          is_causal=causal, scale=scale, enable_gqa=True).numpy()
+
+
+# ----------------------------------------------------------- library cross-checks
+@pytest.mark.parametrize("B,Hq,Hkv,L,D", [(1, 4, 4, 5, 3), (2, 8, 2, 7, 4), (1, 6, 1, 9, 8), (3, 8, 4, 1, 5),
+                                          (2, 12, 3, 16, 16)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_matches_torch_sdpa_gqa(oracle_mod, B, Hq, Hkv, L, D, causal):
+    """Scaled dot-product attention of the Huawei Cloud post (section 5 code)
+    with one K/V head per group; torch's fp64 SDPA with enable_gqa is an
+    independent implementation of the same definition."""
+    _, q = bf16(rnd((B, Hq, L, D), 1))
+    _, k = bf16(rnd((B, Hkv, L, D), 2))
+    _, v = bf16(rnd((B, Hkv, L, D), 3))
+    got = oracle_mod.prefill(q, k, v, causal=causal)
+    ref = sdpa(q, k, v, causal=causal, scale=1 / math.sqrt(D))
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,D", [(2, 8, 2, 9, 4), (3, 4, 1, 6, 3), (1, 4, 4, 12, 8)])
+def test_decode_matches_materialised_repeat_interleave(oracle_mod, B, Hq, Hkv, Lmax, D):
+    """The GQA module of "手把手教你用PyTorch实现GQA" (section 1.3) and
+    `repeat_kv` of the GQA paper notes expand K/V with repeat_interleave over
+    the head axis; after that the computation is plain multi-head attention."""
+    _, q = bf16(rnd((B, Hq, D), 4, 2.0))
+    _, k = bf16(rnd((B, Hkv, Lmax, D), 5))
+    _, v = bf16(rnd((B, Hkv, Lmax, D), 6))
+    seqlens = np.array([Lmax - b for b in range(B)], dtype=np.int32)
+    scale = 0.37
+    got = oracle_mod.decode(q, k, v, seqlens, scale)
+    kx = np.repeat(k, Hq // Hkv, axis=1)  # repeat_interleave on dim 1
+    vx = np.repeat(v, Hq // Hkv, axis=1)
+    for b in range(B):
+        n = seqlens[b]
+        ref = F.scaled_dot_product_attention(torch.from_numpy(q[b][:, None, :]), torch.from_numpy(kx[b, :, :n]),
+                                             torch.from_numpy(vx[b, :, :n]), scale=scale).numpy()[:, 0, :]
+        np.testing.assert_allclose(got[b], ref, rtol=0, atol=1e-13)
+
+
+def test_huawei_demo_shapes(oracle_mod):
+    """The two demos of the Huawei Cloud post: d_model 12 with 4 heads (head
+    size 3) and d_model 32 with 8 heads in groups of 2 (head size 4); a 5-token
+    pass with the cache on (no mask: `masked` defaults to False) then two
+    single-token steps that see the whole cache."""
+    for Hq, D, per_group, seed in ((4, 3, 1, 10), (8, 4, 2, 11)):
+        Hkv = Hq // per_group
+        _, q5 = bf16(rnd((1, Hq, 5, D), seed))
+        _, k7 = bf16(rnd((1, Hkv, 7, D), seed + 1))
+        _, v7 = bf16(rnd((1, Hkv, 7, D), seed + 2))
+        _, qd = bf16(rnd((1, Hq, 2, D), seed + 3))
+        out5 = oracle_mod.prefill(q5, k7[:, :, :5].copy(), v7[:, :, :5].copy(), causal=False)
+        np.testing.assert_allclose(out5, sdpa(q5, k7[:, :, :5], v7[:, :, :5]), atol=1e-13, rtol=0)
+        for step, n in ((0, 6), (1, 7)):
+            o = oracle_mod.decode(qd[:, :, step, :].copy(), k7, v7, np.array([n], np.int32))
+            ref = sdpa(qd[:, :, step:step + 1, :], k7[:, :, :n], v7[:, :, :n])[:, :, 0, :]
+            np.testing.assert_allclose(o, ref, atol=1e-13, rtol=0)
+
+
+# ----------------------------------------------------------- closed forms
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (6, 3), (4, 4), (8, 1)])
+def test_group_constant_values_pin_head_to_group_map(oracle_mod, Hq, Hkv):
+    """Group j's V rows all equal j+1: whatever the weights, head h returns
+    exactly (h div G) + 1 -- the grouping `head_index // n_head_per_group` of
+    the Huawei Cloud post (section 5) and repeat_interleave of section 1.3 of
+    the bjdmk page; the tiling map h mod Hkv would give a different answer."""
+    B, Lmax, D = 2, 11, 4
+    _, q = bf16(rnd((B, Hq, D), 20, 3.0))
+    _, k = bf16(rnd((B, Hkv, Lmax, D), 21))
+    v = np.zeros((B, Hkv, Lmax, D))
+    for j in range(Hkv):
+        v[:, j] = j + 1
+    out = oracle_mod.decode(q, k, v, np.array([Lmax, 5], np.int32))
+    G = Hq // Hkv
+    for h in range(Hq):
+        np.testing.assert_allclose(out[:, h, :], h // G + 1, rtol=1e-14, atol=0)
+    outp = oracle_mod.prefill(np.repeat(q[:, :, None, :], Lmax, axis=2), k, v, causal=True)
+    for h in range(Hq):
+        np.testing.assert_allclose(outp[:, h], h // G + 1, rtol=1e-14, atol=0)
+
+
+def test_constant_values_pin_normalisation(oracle_mod):
+    """Softmax rows sum to one (Huawei Cloud post, softmax over dim -1), so a
+    constant V comes back unchanged."""
+    _, q = bf16(rnd((2, 4, 3, 8), 30, 4.0))
+    _, k = bf16(rnd((2, 2, 3, 8), 31))
+    v = np.full((2, 2, 3, 8), -1.75)
+    for causal in (False, True):
+        np.testing.assert_allclose(oracle_mod.prefill(q, k, v, causal=causal), -1.75, rtol=1e-14, atol=0)
+
+
+def test_single_key_returns_v_exactly(oracle_mod):
+    """softmax of a single logit is exactly 1: a one-key context returns V."""
+    _, q = bf16(rnd((3, 4, 8), 40, 5.0))
+    _, k = bf16(rnd((3, 2, 6, 8), 41))
+    _, v = bf16(rnd((3, 2, 6, 8), 42))
+    out = oracle_mod.decode(q, k, v, np.array([1, 1, 1], np.int32))
+    for h in range(4):
+        np.testing.assert_array_equal(out[:, h], v[:, h // 2, 0])
+
+
+def test_two_key_logistic_closed_form(oracle_mod):
+    """Two keys: the weight of key 0 is the logistic function of the scaled
+    logit gap, sigma(scale (a - b)), with a = <q,k0>, b = <q,k1>."""
+    D = 4
+    q = np.array([[[1.0, 0.5, -2.0, 0.25]]])
+    k = np.array([[[[0.5, 1.0, 0.0, 2.0], [-1.0, 0.0, 0.5, 1.0]]]])
+    v = np.array([[[[1.0, 2.0, 3.0, 4.0], [-4.0, 0.0, 8.0, 0.5]]]])
+    a = float(q[0, 0] @ k[0, 0, 0])
+    b = float(q[0, 0] @ k[0, 0, 1])
+    for scale in (0.5, 1.0 / math.sqrt(D), 3.0):
+        w0 = 1.0 / (1.0 + math.exp(-scale * (a - b)))
+        ref = w0 * v[0, 0, 0] + (1 - w0) * v[0, 0, 1]
+        got = oracle_mod.decode(q, k, v, np.array([2], np.int32), scale)
+        np.testing.assert_allclose(got[0, 0], ref, rtol=1e-14, atol=1e-15)
+
+
+def test_zero_query_gives_mean_of_visible_values(oracle_mod):
+    """q = 0 makes every logit 0: the weights are uniform over visible keys."""
+    _, k = bf16(rnd((1, 1, 9, 4), 50))
+    _, v = bf16(rnd((1, 1, 9, 4), 51))
+    q = np.zeros((1, 3, 4))
+    out = oracle_mod.decode(q, k, v, np.array([6], np.int32))
+    for h in range(3):
+        np.testing.assert_allclose(out[0, h], v[0, 0, :6].mean(axis=0), rtol=1e-14, atol=1e-15)
+
+
+def test_dominant_logit_selects_its_value(oracle_mod):
+    """One logit 50 above all others: its weight is 1 - O(e^-50)."""
+    D, n = 4, 7
+    q = np.zeros((1, 1, D)); q[0, 0, 0] = 1.0
+    k = np.zeros((1, 1, n, D)); k[0, 0, 3, 0] = 50.0
+    _, v = bf16(rnd((1, 1, n, D), 60))
+    out = oracle_mod.decode(q, k, v, np.array([n], np.int32), 1.0)
+    np.testing.assert_allclose(out[0, 0], v[0, 0, 3], rtol=0, atol=1e-12)
+
+
+def test_causal_staircase(oracle_mod):
+    """Causal mask triu(ones, diagonal=1) -> -inf (Huawei Cloud post): with
+    K = 0 every visible key weighs the same, so with V[t] = t row i returns
+    the mean of 0..i = i/2 -- the diagonal key is visible, later ones are not.
+    Row 0 returns v_0 exactly."""
+    L, D = 9, 3
+    _, q = bf16(rnd((1, 2, L, D), 70, 2.0))
+    k = np.zeros((1, 1, L, D))
+    v = np.repeat(np.arange(L, dtype=np.float64)[None, None, :, None], D, axis=3)
+    out = oracle_mod.prefill(q, k, v, causal=True)
+    for i in range(L):
+        np.testing.assert_allclose(out[0, :, i], i / 2, rtol=1e-14, atol=1e-15)
+    _, k2 = bf16(rnd((1, 1, L, D), 71))
+    _, v2 = bf16(rnd((1, 1, L, D), 72))
+    out2 = oracle_mod.prefill(q, k2, v2, causal=True)
+    np.testing.assert_array_equal(out2[0, :, 0], np.repeat(v2[0, :, 0], 2, axis=0))
+
+
+def test_causal_rows_ignore_future_keys(oracle_mod):
+    """Changing K/V at positions t > i leaves row i unchanged (bit for bit)."""
+    L, D = 10, 8
+    _, q = bf16(rnd((2, 4, L, D), 80))
+    _, k = bf16(rnd((2, 2, L, D), 81))
+    _, v = bf16(rnd((2, 2, L, D), 82))
+    base = oracle_mod.prefill(q, k, v, causal=True)
+    for i in (0, 3, 8):
+        k2, v2 = k.copy(), v.copy()
+        k2[:, :, i + 1:] = 1e3
+        v2[:, :, i + 1:] = -7.0
+        pert = oracle_mod.prefill(q, k2, v2, causal=True)
+        np.testing.assert_array_equal(pert[:, :, : i + 1], base[:, :, : i + 1])
+
+
+# ----------------------------------------------------------- invariants
+def test_mha_endpoint_is_per_head_attention(oracle_mod):
+    """GQA-H (Hkv = Hq) is MHA (GQA paper notes): each head is an independent
+    single-head attention over its own K/V."""
+    B, H, L, D = 2, 4, 6, 8
+    _, q = bf16(rnd((B, H, L, D), 90))
+    _, k = bf16(rnd((B, H, L, D), 91))
+    _, v = bf16(rnd((B, H, L, D), 92))
+    full = oracle_mod.prefill(q, k, v, causal=True)
+    for h in range(H):
+        one = oracle_mod.prefill(q[:, h:h + 1].copy(), k[:, h:h + 1].copy(), v[:, h:h + 1].copy(), causal=True)
+        np.testing.assert_array_equal(full[:, h:h + 1], one)
+
+
+def test_mqa_endpoint_is_broadcast(oracle_mod):
+    """GQA-1 is MQA (GQA paper notes; the MQA module of the bjdmk page
+    broadcasts one K/V head with unsqueeze(1)): Hkv = 1 equals MHA on the
+    K/V head copied to every query head."""
+    B, H, Lmax, D = 2, 6, 8, 4
+    _, q = bf16(rnd((B, H, D), 93))
+    _, k = bf16(rnd((B, 1, Lmax, D), 94))
+    _, v = bf16(rnd((B, 1, Lmax, D), 95))
+    sl = np.array([8, 3], np.int32)
+    mqa = oracle_mod.decode(q, k, v, sl)
+    mha = oracle_mod.decode(q, np.repeat(k, H, axis=1), np.repeat(v, H, axis=1), sl)
+    np.testing.assert_array_equal(mqa, mha)
+
+
+def test_decode_is_last_row_of_causal_prefill(oracle_mod):
+    """A decode step of the token at position n-1 over n cached keys is row
+    n-1 of a causal pass over those n tokens."""
+    B, Hq, Hkv, n, D = 2, 8, 2, 7, 8
+    _, q = bf16(rnd((B, Hq, n, D), 96))
+    _, k = bf16(rnd((B, Hkv, n, D), 97))
+    _, v = bf16(rnd((B, Hkv, n, D), 98))
+    pre = oracle_mod.prefill(q, k, v, causal=True)
+    dec = oracle_mod.decode(q[:, :, n - 1, :].copy(), k, v, np.array([n, n], np.int32))
+    np.testing.assert_allclose(dec, pre[:, :, n - 1], rtol=0, atol=1e-15)
+
+
+def test_nan_tail_is_not_read(oracle_mod):
+    """Rows at or past seqlens[b] are outside the context: NaN there changes nothing."""
+    B, Hq, Hkv, Lmax, D = 2, 4, 2, 10, 8
+    _, q = bf16(rnd((B, Hq, D), 99))
+    _, k = bf16(rnd((B, Hkv, Lmax, D), 100))
+    _, v = bf16(rnd((B, Hkv, Lmax, D), 101))
+    sl = np.array([4, 10], np.int32)
+    clean = oracle_mod.decode(q, k, v, sl)
+    k[0, :, 4:] = np.nan
+    v[0, :, 4:] = np.nan
+    np.testing.assert_array_equal(oracle_mod.decode(q, k, v, sl), clean)
+
+
+def test_empty_context_is_flagged_and_zero(oracle_mod):
+    _, q = bf16(rnd((2, 2, 4), 102))
+    _, k = bf16(rnd((2, 1, 3, 4), 103))
+    out = oracle_mod.decode(q, k, k, np.array([0, 3], np.int32), check=False)
+    assert np.all(out[0] == 0)
+    with pytest.raises(ValueError):
+        oracle_mod.decode(q, k, k, np.array([0, 3], np.int32))
+
+
+def test_bf16_widening_is_exact(oracle_mod):
+    """bf16 inputs given as bit patterns give the same result as their exact
+    fp64 values (0x3F80 = 1.0, 0xC020 = -2.5, 0x3E00 = 0.125, 0x4120 = 10.0)."""
+    bits = np.array([0x3F80, 0xC020, 0x3E00, 0x4120], dtype=np.uint16)
+    vals = np.array([1.0, -2.5, 0.125, 10.0])
+    q_b = bits.reshape(1, 1, 4); q_f = vals.reshape(1, 1, 4)
+    k_b = np.tile(bits, 3).reshape(1, 1, 3, 4); k_f = np.tile(vals, 3).reshape(1, 1, 3, 4)
+    v_b = np.roll(k_b, 1); v_f = np.roll(k_f, 1)
+    a = oracle_mod.decode(q_b, k_b, v_b, np.array([3], np.int32), 0.01)
+    b = oracle_mod.decode(q_f, k_f, v_f, np.array([3], np.int32), 0.01)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_sampled_rows_equal_full_evaluation(oracle_mod):
+    """Evaluating a subset of rows gives the same rows as the full pass."""
+    w = W.DecodeWorkload("t", 3, 8, 2, 16, 20, 5, 20, 7)
+    q, k, v, sl = W.make_decode_inputs(w)
+    full = oracle_mod.decode(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), sl.numpy())
+    rows = np.array([[2, 7], [0, 0], [1, 3]])
+    part = oracle_mod.decode(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), sl.numpy(), rows=rows)
+    for r, (b, h) in enumerate(rows):
+        np.testing.assert_array_equal(part[r], full[b, h])
+    qp, kp, vp = W.make_prefill_inputs(W.PrefillWorkload("p", 1, 9, 4, 2, 8, True, 8))
+    fullp = oracle_mod.prefill(W.bf16_bits(qp), W.bf16_bits(kp), W.bf16_bits(vp))
+    rows3 = np.array([[0, 3, 8], [0, 0, 0], [0, 2, 4]])
+    partp = oracle_mod.prefill(W.bf16_bits(qp), W.bf16_bits(kp), W.bf16_bits(vp), rows=rows3)
+    for r, (b, h, i) in enumerate(rows3):
+        np.testing.assert_array_equal(partp[r], fullp[b, h, i])
