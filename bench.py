@@ -1,0 +1,391 @@
+"""Benchmark of the grouped-query attention hot path on B300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gqa,reference}]
+
+A step is one gqa_decode call (split-KV partial attention, the in-kernel
+log-sum-exp merge, over the bf16 [B, Hkv, Lmax, D] cache) on the Llama-3-8B
+shaped workload B=16, Hq=32, Hkv=8, D=128, L=4096, inputs resident in HBM.
+The headline value is K/V bytes read per second (the visible cache rows, once
+per KV head) -- decode is bound by reading the KV cache.  The causal prefill
+(B=4, L=2048, Hq=32, Hkv=8, D=128) is timed in the same run and reported in
+TFLOP/s under "prefill"; the other decode workloads under "decode_workloads".
+
+L2 (126 MB) is flushed by writing a 256 MiB buffer before every timed launch;
+each launch is bracketed by its own CUDA events on the launching stream, and
+ms_per_step is the mean of those event intervals.
+
+Under torchrun (N > 1) every rank runs its own batch of the same shape
+(independent sequences: no data-path collective; weak scaling); the value is
+the bytes of all ranks divided by the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle on the same workload, metric and
+unit (a bounded sample of (b, h) rows, extrapolated to the full step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GQA decode K/V-read GB/s (% HBM peak); causal prefill TFLOP/s; 1xB300"
+HEADLINE = "llama3_8b"
+
+# DRAM bytes (read + write) per launch from one ncu capture, keyed by the
+# SHA-256 of the kernel source they were taken on; reported as null as soon
+# as the source differs.
+NCU_TRAFFIC = {}
+
+
+def _sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def traffic_for(kernel_file, scale=1.0):
+    rec = NCU_TRAFFIC.get(os.path.basename(kernel_file))
+    if not rec or rec["sha256"] != _sha(kernel_file):
+        return None
+    return rec["bytes_per_launch"] * scale
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ timing
+def timed_launches(fn, steps, warmup, flush, stream):
+    """Runs fn() warmup times, then `steps` times with an L2 flush before each
+    launch; returns the per-launch event durations in ms."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def bench_decode(g, W, name, dev, steps, warmup, flush, seed_offset=0):
+    import torch
+    w = W.WORKLOADS[name]
+    if seed_offset:
+        w = W.DecodeWorkload(w.name, w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.len_lo, w.len_hi, w.seed + seed_offset)
+    q, k, v, sl = W.make_decode_inputs(w)
+    qd, kd, vd, sld = q.to(dev), k.to(dev), v.to(dev), sl.to(dev)
+    out = torch.empty_like(qd)
+    stream = torch.cuda.current_stream(dev)
+    ts = timed_launches(lambda: g.gqa_decode(qd, kd, vd, sld, out=out, scale=w.scale, stream=stream),
+                        steps, warmup, flush, stream)
+    flags = g.gqa_get_device_status()
+    if flags:
+        raise RuntimeError(f"decode {name}: device status {flags:#x}")
+    nbytes = W.decode_kv_bytes(sl, w.Hkv, w.D)
+    return {"w": w, "inputs": (q, k, v, sl), "ms": ts, "bytes": nbytes,
+            "flops": W.decode_flops(sl, w.Hq, w.D)}
+
+
+def bench_prefill(g, W, dev, steps, warmup, flush):
+    import torch
+    w = W.WORKLOADS["prefill"]
+    q, k, v = W.make_prefill_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty_like(qd)
+    stream = torch.cuda.current_stream(dev)
+    try:
+        g.gqa_prefill(qd, kd, vd, out=out, causal=w.causal, stream=stream)
+    except g.GQAError as e:
+        if e.status == g.GQA_ERR_UNSUPPORTED:
+            return None
+        raise
+    ts = timed_launches(lambda: g.gqa_prefill(qd, kd, vd, out=out, causal=w.causal, stream=stream),
+                        steps, warmup, flush, stream)
+    return {"w": w, "ms": ts, "flops": W.prefill_flops(w.B, w.Hq, w.L, w.D, w.causal)}
+
+
+def e2e_decode(g, W, name, steps, warmup):
+    """Same metric through gqa_decode_host: pinned host inputs copied in and the
+    output copied back inside the timed region, every step."""
+    import torch
+    w = W.WORKLOADS[name]
+    q, k, v, sl = W.make_decode_inputs(w)
+    q, k, v, sl = q.pin_memory(), k.pin_memory(), v.pin_memory(), sl.pin_memory()
+    out = torch.empty_like(q).pin_memory()
+    for _ in range(warmup):
+        g.gqa_decode_host(q, k, v, sl, out=out, scale=w.scale)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        g.gqa_decode_host(q, k, v, sl, out=out, scale=w.scale)
+    dt = (time.perf_counter() - t0) / steps
+    nbytes = W.decode_kv_bytes(sl, w.Hkv, w.D)
+    h2d = q.numel() * 2 + k.numel() * 2 + v.numel() * 2 + sl.numel() * 4
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": dt * 1e3}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_decode_rate(W, name, budget_s=12.0, max_rows=None):
+    """fp64 oracle on the host cores: time a sample of (b, h) rows, extrapolate
+    to the whole step and return (GB/s of the step's K/V bytes, sample text, threads)."""
+    import numpy as np
+    import oracle
+    w = W.WORKLOADS[name]
+    q, k, v, sl = W.make_decode_inputs(w)
+    qb, kb, vb, sln = W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), sl.numpy()
+    rows_all = np.array([(b, h) for b in range(w.B) for h in range(w.Hq)], dtype=np.int32)
+    n = 8
+    elapsed, done = 0.0, 0
+    while elapsed < budget_s and done < len(rows_all):
+        take = rows_all[done:done + n] if max_rows is None else rows_all[done:done + min(n, max_rows - done)]
+        if len(take) == 0:
+            break
+        t0 = time.perf_counter()
+        oracle.decode(qb, kb, vb, sln, w.scale, rows=take)
+        elapsed += time.perf_counter() - t0
+        done += len(take)
+        n = min(n * 2, 256)
+        if max_rows is not None and done >= max_rows:
+            break
+    rows_per_s = done / elapsed
+    step_s = len(rows_all) / rows_per_s
+    nbytes = W.decode_kv_bytes(sl, w.Hkv, w.D)
+    sample = f"{done} of {len(rows_all)} (b, h) rows of one step in {elapsed:.1f} s, extrapolated to the step"
+    return nbytes / step_s / 1e9, step_s, sample, oracle.num_threads()
+
+
+# ------------------------------------------------------------------ main
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("GQA_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def max_over_ranks(x, world, dev=None):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev if dev is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from grouped_query_attention_09_b300 import workloads as W
+    steps = []
+    for _ in range(args.warmup):
+        oracle_decode_rate(W, HEADLINE, budget_s=1.0, max_rows=16)
+    sample = threads = None
+    for _ in range(args.steps):
+        gbs, step_s, sample, threads = oracle_decode_rate(W, HEADLINE, budget_s=args.ref_budget)
+        steps.append(step_s)
+    step_s = statistics.mean(steps)
+    w = W.WORKLOADS[HEADLINE]
+    nbytes = W.decode_kv_bytes(W.make_decode_inputs(W.DecodeWorkload("x", w.B, w.Hq, w.Hkv, w.D, 1, 1, 1, 0))[3]
+                               * w.len_lo, w.Hkv, w.D)
+    value = nbytes / step_s / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama3_8b decode: B=16, Hq=32, Hkv=8, D=128, L=4096, bf16 inputs widened to fp64",
+                       "reference": "fp64 CPU oracle (oracle/gqa_oracle.c), no installable reference exists"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gqa", choices=["gqa", "reference"])
+    ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="headline only (for profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        rc = run_reference(args, rank, world)
+        barrier(world)
+        return rc
+
+    import torch
+    import grouped_query_attention_09_b300 as g
+    from grouped_query_attention_09_b300 import workloads as W
+
+    g.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+
+    barrier(world)
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        res = bench_decode(g, W, HEADLINE, dev, args.steps, args.warmup, flush, seed_offset=rank)
+        torch.cuda.synchronize()
+    barrier(world)
+    mean_ms = statistics.mean(res["ms"])
+    total_ms = max_over_ranks(sum(res["ms"]), world, dev)
+    value = res["bytes"] * world * args.steps / (total_ms / 1e3) / 1e9
+    achieved = res["bytes"] / (mean_ms / 1e3) / 1e9
+
+    extras = {}
+    if not args.no_extras:
+        small_steps = max(50, min(args.steps, 400))
+        dw = {}
+        for name in ("tiny", "llama2_70b", "mqa"):
+            r = bench_decode(g, W, name, dev, small_steps, args.warmup, flush)
+            ms = statistics.mean(r["ms"])
+            gbs = r["bytes"] / (ms / 1e3) / 1e9
+            dw[name] = {"us": ms * 1e3, "kv_bytes": r["bytes"], "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+                        "TFLOP/s": r["flops"] / (ms / 1e3) / 1e12}
+        dw[HEADLINE] = {"us": mean_ms * 1e3, "kv_bytes": res["bytes"], "GB/s": achieved,
+                        "frac_hbm": achieved / peaks["hbm_gbs"], "TFLOP/s": res["flops"] / (mean_ms / 1e3) / 1e12}
+        extras["decode_workloads"] = dw
+        pr = bench_prefill(g, W, dev, small_steps, args.warmup, flush)
+        if pr is not None:
+            pms = statistics.mean(pr["ms"])
+            tf = pr["flops"] / (pms / 1e3) / 1e12
+            extras["prefill"] = {
+                "workload": "causal prefill: B=4, L=2048, Hq=32, Hkv=8, D=128", "us": pms * 1e3,
+                "flops": pr["flops"], "TFLOP/s": tf,
+                "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": tf / peaks["bf16_tflops"],
+                             "frac_sustained": tf / peaks["bf16_tflops_sustained"]
+                             if peaks.get("bf16_tflops_sustained") else None,
+                             "traffic": traffic_for(os.path.join(ROOT, "grouped_query_attention_09_b300", "csrc",
+                                                                 "prefill.cu"))}}
+        else:
+            extras["prefill"] = {"status": "not built"}
+        if rank == 0:
+            extras["e2e"] = e2e_decode(g, W, HEADLINE, steps=max(5, min(args.steps, 20)), warmup=2)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, step_s, sample, threads = oracle_decode_rate(W, HEADLINE, budget_s=12.0)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "llama3_8b decode: B=16, Hq=32, Hkv=8, D=128, L=4096 (bf16 KV cache "
+                                   "[16, 8, 4096, 128] + q [16, 32, 128], N(0,1) seed 2)",
+                       "l2": "flushed (256 MiB write) before every timed launch",
+                       "parallelism": f"replica per GPU x{world}" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                         "kernel": "decode_kernel<128,1>",
+                         "traffic": traffic_for(os.path.join(ROOT, "grouped_query_attention_09_b300", "csrc",
+                                                             "decode.cu"))},
+            "cpu_baseline": cpu,
+            "e2e": extras.pop("e2e", None),
+            "gpu_launches": args.steps,
+            "clocks": clocks.summary(),
+        }
+        line.update(extras)
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,198 @@
+"""Grouped-query attention on NVIDIA B300 (sm_103a).
+
+A thin ctypes binding of libgqa.so: every function here only marshals
+arguments (torch tensors -> raw pointers and sizes) and raises on a non-zero
+status.  All arithmetic runs in the library's CUDA kernels; there is no CPU
+or PyTorch fallback, and a missing or unloadable library raises.
+
+Names and semantics follow include/gqa.h:
+  gqa_decode, gqa_prefill, gqa_decode_host, gqa_prefill_host,
+  gqa_status_string, gqa_get_device_status, gqa_decode_plan, gqa_release.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgqa.so")
+
+GQA_OK = 0
+GQA_ERR_INVALID_ARG = 1
+GQA_ERR_UNSUPPORTED = 2
+GQA_ERR_NULL = 3
+GQA_ERR_MISALIGNED = 4
+GQA_ERR_CUDA = 5
+GQA_ERR_NO_DEVICE = 6
+
+GQA_DEV_SEQLEN_CLAMPED = 0x1
+GQA_DEV_EMPTY_CONTEXT = 0x2
+GQA_DEV_WAIT_TIMEOUT = 0x4
+
+EXPORTED = ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host",
+            "gqa_status_string", "gqa_get_device_status", "gqa_decode_plan", "gqa_release")
+
+_lib = None
+
+
+class GQAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gqa_status_string(status)}")
+
+
+def load_library():
+    """Loads libgqa.so (built by grouped_query_attention_09_b300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: run `python -m grouped_query_attention_09_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.gqa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.gqa_prefill.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
+    lib.gqa_decode_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.gqa_prefill_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
+    for fn in ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host"):
+        getattr(lib, fn).restype = i
+    lib.gqa_status_string.argtypes = [i]
+    lib.gqa_status_string.restype = ctypes.c_char_p
+    lib.gqa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.gqa_get_device_status.restype = i
+    lib.gqa_decode_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+    lib.gqa_decode_plan.restype = i
+    lib.gqa_release.argtypes = []
+    lib.gqa_release.restype = None
+    _lib = lib
+    return lib
+
+
+def gqa_status_string(status: int) -> str:
+    return load_library().gqa_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != GQA_OK:
+        raise GQAError(status, where)
+
+
+def _stream_ptr(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev_ptr(t, name, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def gqa_decode(q, k_cache, v_cache, seqlens, out=None, scale=None, stream=None):
+    """One decode step.  q [B, Hq, D] bf16; k_cache/v_cache [B, Hkv, Lmax, D]
+    bf16; seqlens [B] int32 (device); returns out [B, Hq, D] bf16."""
+    import torch
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = D ** -0.5
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.gqa_decode(_dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k_cache, "k_cache", torch.bfloat16),
+                            _dev_ptr(v_cache, "v_cache", torch.bfloat16), _dev_ptr(seqlens, "seqlens", torch.int32),
+                            _dev_ptr(out, "out", torch.bfloat16), B, Hq, Hkv, D, Lmax, float(scale),
+                            _stream_ptr(stream, q.device))
+    _check(st, "gqa_decode")
+    return out
+
+
+def gqa_prefill(q, k, v, out=None, causal=True, stream=None):
+    """Prefill.  q [B, Hq, L, D], k/v [B, Hkv, L, D] bf16; returns out like q."""
+    import torch
+    B, Hq, L, D = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.gqa_prefill(_dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k, "k", torch.bfloat16),
+                             _dev_ptr(v, "v", torch.bfloat16), _dev_ptr(out, "out", torch.bfloat16),
+                             B, L, Hq, Hkv, D, int(bool(causal)), _stream_ptr(stream, q.device))
+    _check(st, "gqa_prefill")
+    return out
+
+
+def _host_ptr(t, name, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a CPU tensor")
+    if t.dtype != dtype or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous {dtype} tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def gqa_decode_host(q, k_cache, v_cache, seqlens, out=None, scale=None, stream=None, device=None):
+    """gqa_decode on host (CPU, ideally pinned) tensors; returns a host out."""
+    import torch
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = D ** -0.5
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        st = load_library().gqa_decode_host(
+            _host_ptr(q, "q", torch.bfloat16), _host_ptr(k_cache, "k_cache", torch.bfloat16),
+            _host_ptr(v_cache, "v_cache", torch.bfloat16), _host_ptr(seqlens, "seqlens", torch.int32),
+            _host_ptr(out, "out", torch.bfloat16), B, Hq, Hkv, D, Lmax, float(scale), _stream_ptr(stream, device))
+    _check(st, "gqa_decode_host")
+    return out
+
+
+def gqa_prefill_host(q, k, v, out=None, causal=True, stream=None, device=None):
+    """gqa_prefill on host tensors; returns a host out."""
+    import torch
+    B, Hq, L, D = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        st = load_library().gqa_prefill_host(
+            _host_ptr(q, "q", torch.bfloat16), _host_ptr(k, "k", torch.bfloat16), _host_ptr(v, "v", torch.bfloat16),
+            _host_ptr(out, "out", torch.bfloat16), B, L, Hq, Hkv, D, int(bool(causal)), _stream_ptr(stream, device))
+    _check(st, "gqa_prefill_host")
+    return out
+
+
+def gqa_get_device_status(stream=None, device=None) -> int:
+    """Synchronises the stream and returns (and clears) the GQA_DEV_* bits."""
+    import torch
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    flags = ctypes.c_uint32(0)
+    with torch.cuda.device(device):
+        st = load_library().gqa_get_device_status(_stream_ptr(stream, device), ctypes.byref(flags))
+    _check(st, "gqa_get_device_status")
+    return int(flags.value)
+
+
+def gqa_decode_plan(B, Hq, Hkv, D, Lmax):
+    """(tile_keys, num_ctas) of the split gqa_decode would use."""
+    tk, nc = ctypes.c_int(0), ctypes.c_int(0)
+    st = load_library().gqa_decode_plan(B, Hq, Hkv, D, Lmax, ctypes.byref(tk), ctypes.byref(nc))
+    _check(st, "gqa_decode_plan")
+    return tk.value, nc.value
+
+
+def gqa_release():
+    load_library().gqa_release()

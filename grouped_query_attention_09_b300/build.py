@@ -1,0 +1,62 @@
+"""Builds libgqa.so (the CUDA kernels and the C ABI) in-tree for sm_103a.
+
+Usage: python -m grouped_query_attention_09_b300.build [--force]
+The library links the CUDA runtime statically and reaches the driver API
+only through cudaGetDriverEntryPointByVersion, so it loads (and exports its
+symbols) on a machine without a GPU driver; every compute call then reports
+GQA_ERR_NO_DEVICE.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
+LIB = os.path.join(HERE, "libgqa.so")
+SOURCES = ["api.cu", "decode.cu", "prefill.cu"]
+HEADERS = ["ptx.cuh", "internal.h", "tcgen05.cuh"]
+
+NVCC_FLAGS = [
+    "-gencode", "arch=compute_103a,code=sm_103a",
+    "-O3", "-lineinfo", "-std=c++17",
+    "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+    "-Xptxas", "-v",
+]
+
+
+def _inputs():
+    files = [os.path.join(CSRC, s) for s in SOURCES]
+    files += [os.path.join(CSRC, h) for h in HEADERS if os.path.exists(os.path.join(CSRC, h))]
+    files.append(os.path.join(INCLUDE, "gqa.h"))
+    return files
+
+
+def up_to_date() -> bool:
+    if not os.path.exists(LIB):
+        return False
+    t = os.path.getmtime(LIB)
+    return all(os.path.getmtime(f) <= t for f in _inputs())
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    if not force and up_to_date():
+        return LIB
+    nvcc = os.environ.get("NVCC", "nvcc")
+    tmp = LIB + f".tmp{os.getpid()}"
+    cmd = [nvcc, *NVCC_FLAGS, "-shared", "-I", INCLUDE,
+           *[os.path.join(CSRC, s) for s in SOURCES], "-o", tmp]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
+    if verbose:
+        sys.stdout.write(res.stdout + res.stderr)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    build(force="--force" in sys.argv, verbose=True)
+    print(LIB)

@@ -1,0 +1,357 @@
+// api.cu -- the extern "C" boundary of libgqa.so: argument checks, per-device
+// workspace, tensor-map encoding, host-buffer variants and status reporting.
+// Declarations and their contracts are in include/gqa.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/gqa.h"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_cuda_msg;
+std::mutex g_mu;
+
+struct DeviceCtx {
+  bool ready = false;
+  int sm_count = 0;
+  float* ws_part = nullptr;
+  size_t ws_part_cap = 0;
+  int* counters = nullptr;
+  size_t counters_cap = 0;
+  unsigned* err = nullptr;
+  cudaEvent_t last_evt = nullptr;
+  cudaStream_t last_stream = nullptr;
+  bool evt_pending = false;
+  void* stage = nullptr;  // host-call staging
+  size_t stage_cap = 0;
+};
+std::vector<DeviceCtx> g_dev;
+
+int cuda_fail(cudaError_t e) {
+  g_cuda_msg = std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e);
+  return GQA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Current device's context, created on first use.  Caller holds g_mu.
+int get_ctx(DeviceCtx** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cuda_fail(e);
+    return GQA_ERR_NO_DEVICE;
+  }
+  if ((int)g_dev.size() <= dev) g_dev.resize(dev + 1);
+  DeviceCtx& c = g_dev[dev];
+  if (!c.ready) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&c.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if (major != 10 || minor != 3) {
+      g_cuda_msg = "device is sm_" + std::to_string(major) + std::to_string(minor) +
+                   "; libgqa.so is built for sm_103a only";
+      return GQA_ERR_NO_DEVICE;
+    }
+    if ((e = cudaMalloc(&c.err, sizeof(unsigned))) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemset(c.err, 0, sizeof(unsigned))) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaEventCreateWithFlags(&c.last_evt, cudaEventDisableTiming)) != cudaSuccess)
+      return cuda_fail(e);
+    c.ready = true;
+  }
+  *out = &c;
+  return GQA_OK;
+}
+
+// Orders this call after the previous workspace user if it ran on another stream.
+cudaError_t order_after_previous(DeviceCtx& c, cudaStream_t s) {
+  if (c.evt_pending && c.last_stream != s) return cudaStreamWaitEvent(s, c.last_evt, 0);
+  return cudaSuccess;
+}
+
+cudaError_t mark_used(DeviceCtx& c, cudaStream_t s) {
+  c.last_stream = s;
+  c.evt_pending = true;
+  return cudaEventRecord(c.last_evt, s);
+}
+
+int check_decode_args(const void* q, const void* k, const void* v, const int32_t* seqlens,
+                      const void* out, int B, int Hq, int Hkv, int D, int Lmax, float scale) {
+  if (!q || !k || !v || !seqlens || !out) return GQA_ERR_NULL;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+    return GQA_ERR_MISALIGNED;
+  gqa::DecodePlan plan;
+  if (!gqa::decode_plan(B, Hq, Hkv, D, Lmax, 148, &plan)) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+int check_prefill_args(const void* q, const void* k, const void* v, const void* out, int B, int L,
+                       int Hq, int Hkv, int D, int causal) {
+  if (!q || !k || !v || !out) return GQA_ERR_NULL;
+  if (B <= 0 || L <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return GQA_ERR_MISALIGNED;
+  if (!gqa::prefill_supported(D)) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+int decode_locked(DeviceCtx& c, const void* q, const void* k, const void* v, const int32_t* seqlens,
+                  void* out, int B, int Hq, int Hkv, int D, int Lmax, float scale, cudaStream_t s) {
+  gqa::DecodePlan plan;
+  if (!gqa::decode_plan(B, Hq, Hkv, D, Lmax, c.sm_count, &plan)) return GQA_ERR_UNSUPPORTED;
+  cudaError_t e;
+  if (plan.ws_part_floats > c.ws_part_cap || plan.ws_counters > c.counters_cap) {
+    // Growing the workspace: cudaFree waits for work that still uses the old one.
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+    if (plan.ws_part_floats > c.ws_part_cap) {
+      if (c.ws_part) cudaFree(c.ws_part);
+      c.ws_part = nullptr;
+      c.ws_part_cap = 0;
+      if ((e = cudaMalloc(&c.ws_part, plan.ws_part_floats * sizeof(float))) != cudaSuccess) return cuda_fail(e);
+      c.ws_part_cap = plan.ws_part_floats;
+    }
+    if (plan.ws_counters > c.counters_cap) {
+      if (c.counters) cudaFree(c.counters);
+      c.counters = nullptr;
+      c.counters_cap = 0;
+      if ((e = cudaMalloc(&c.counters, plan.ws_counters * sizeof(int))) != cudaSuccess) return cuda_fail(e);
+      if ((e = cudaMemset(c.counters, 0, plan.ws_counters * sizeof(int))) != cudaSuccess) return cuda_fail(e);
+      c.counters_cap = plan.ws_counters;
+    }
+  }
+  if ((e = order_after_previous(c, s)) != cudaSuccess) return cuda_fail(e);
+  gqa::DecodeArgs a{q, k, v, seqlens, out, B, Hq, Hkv, D, Lmax, scale, c.ws_part, c.counters, c.err};
+  if ((e = gqa::decode_launch(plan, a, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = mark_used(c, s)) != cudaSuccess) return cuda_fail(e);
+  return GQA_OK;
+}
+
+cudaError_t ensure_stage(DeviceCtx& c, size_t bytes, cudaStream_t s) {
+  if (bytes <= c.stage_cap) return cudaSuccess;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  if (c.stage) cudaFree(c.stage);
+  c.stage = nullptr;
+  c.stage_cap = 0;
+  if ((e = cudaMalloc(&c.stage, bytes)) != cudaSuccess) return e;
+  c.stage_cap = bytes;
+  return cudaSuccess;
+}
+
+size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+namespace gqa {
+
+CUresult encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1,
+                             uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
+                             uint32_t box1, uint32_t box2) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t dims[3] = {dim0, dim1, dim2};
+  cuuint64_t strides[2] = {stride1, stride2};
+  cuuint32_t box[3] = {box0, box1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace gqa
+
+extern "C" {
+
+int gqa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens,
+               void* out, int B, int Hq, int Hkv, int D, int Lmax, float scale, void* stream) {
+  int st = check_decode_args(q, k_cache, v_cache, seqlens, out, B, Hq, Hkv, D, Lmax, scale);
+  if (st != GQA_OK) return st;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceCtx* c = nullptr;
+  if ((st = get_ctx(&c)) != GQA_OK) return st;
+  return decode_locked(*c, q, k_cache, v_cache, seqlens, out, B, Hq, Hkv, D, Lmax, scale,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int gqa_prefill(const void* q, const void* k, const void* v, void* out, int B, int L, int Hq, int Hkv,
+                int D, int causal, void* stream) {
+  int st = check_prefill_args(q, k, v, out, B, L, Hq, Hkv, D, causal);
+  if (st != GQA_OK) return st;
+  DeviceCtx* c = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = get_ctx(&c)) != GQA_OK) return st;
+  }
+  gqa::PrefillArgs a{q, k, v, out, B, L, Hq, Hkv, D, causal, c->err};
+  cudaError_t e = gqa::prefill_launch(a, c->sm_count, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
+int gqa_decode_host(const void* q_host, const void* k_cache_host, const void* v_cache_host,
+                    const int32_t* seqlens_host, void* out_host, int B, int Hq, int Hkv, int D,
+                    int Lmax, float scale, void* stream) {
+  if (!q_host || !k_cache_host || !v_cache_host || !seqlens_host || !out_host) return GQA_ERR_NULL;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  gqa::DecodePlan plan;
+  if (!gqa::decode_plan(B, Hq, Hkv, D, Lmax, 148, &plan)) return GQA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t qb = (size_t)B * Hq * D * 2, kb = (size_t)B * Hkv * Lmax * D * 2, sb = (size_t)B * 4;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceCtx* c = nullptr;
+  int st = get_ctx(&c);
+  if (st != GQA_OK) return st;
+  cudaError_t e;
+  if ((e = ensure_stage(*c, al256(qb) * 2 + al256(kb) * 2 + al256(sb), s)) != cudaSuccess) return cuda_fail(e);
+  char* base = static_cast<char*>(c->stage);
+  char* dq = base;
+  char* dk = dq + al256(qb);
+  char* dv = dk + al256(kb);
+  char* dsl = dv + al256(kb);
+  char* dout = dsl + al256(sb);
+  if ((e = order_after_previous(*c, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(dk, k_cache_host, kb, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(dv, v_cache_host, kb, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(dsl, seqlens_host, sb, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e);
+  st = decode_locked(*c, dq, dk, dv, reinterpret_cast<const int32_t*>(dsl), dout, B, Hq, Hkv, D, Lmax,
+                     scale, s);
+  if (st != GQA_OK) return st;
+  if ((e = cudaMemcpyAsync(out_host, dout, qb, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+  return GQA_OK;
+}
+
+int gqa_prefill_host(const void* q_host, const void* k_host, const void* v_host, void* out_host, int B,
+                     int L, int Hq, int Hkv, int D, int causal, void* stream) {
+  if (!q_host || !k_host || !v_host || !out_host) return GQA_ERR_NULL;
+  if (B <= 0 || L <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return GQA_ERR_INVALID_ARG;
+  if (!gqa::prefill_supported(D)) return GQA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t qb = (size_t)B * Hq * L * D * 2, kb = (size_t)B * Hkv * L * D * 2;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceCtx* c = nullptr;
+  int st = get_ctx(&c);
+  if (st != GQA_OK) return st;
+  cudaError_t e;
+  if ((e = ensure_stage(*c, al256(qb) * 2 + al256(kb) * 2, s)) != cudaSuccess) return cuda_fail(e);
+  char* dq = static_cast<char*>(c->stage);
+  char* dk = dq + al256(qb);
+  char* dv = dk + al256(kb);
+  char* dout = dv + al256(kb);
+  if ((e = order_after_previous(*c, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(dk, k_host, kb, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(dv, v_host, kb, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e);
+  gqa::PrefillArgs a{dq, dk, dv, dout, B, L, Hq, Hkv, D, causal, c->err};
+  if ((e = gqa::prefill_launch(a, c->sm_count, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = mark_used(*c, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaMemcpyAsync(out_host, dout, qb, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+  return GQA_OK;
+}
+
+const char* gqa_status_string(int status) {
+  switch (status) {
+    case GQA_OK: return "GQA_OK";
+    case GQA_ERR_INVALID_ARG: return "GQA_ERR_INVALID_ARG: a size is <= 0, Hq % Hkv != 0, causal is not 0/1 or scale is not finite and > 0";
+    case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED: shape not implemented (decode: D in {64,128}, Hq/Hkv <= 8, 16 or 32, B <= 1024; prefill: D == 128)";
+    case GQA_ERR_NULL: return "GQA_ERR_NULL: a required pointer is NULL";
+    case GQA_ERR_MISALIGNED: return "GQA_ERR_MISALIGNED: tensor pointers must be 16-byte aligned (seqlens 4-byte)";
+    case GQA_ERR_CUDA: {
+      static thread_local std::string s;
+      s = "GQA_ERR_CUDA: " + (g_cuda_msg.empty() ? std::string("unknown CUDA error") : g_cuda_msg);
+      return s.c_str();
+    }
+    case GQA_ERR_NO_DEVICE: {
+      static thread_local std::string s;
+      s = "GQA_ERR_NO_DEVICE: " + (g_cuda_msg.empty() ? std::string("no sm_103 device") : g_cuda_msg);
+      return s.c_str();
+    }
+    default: return "unknown gqa status";
+  }
+}
+
+int gqa_get_device_status(void* stream, uint32_t* flags) {
+  if (!flags) return GQA_ERR_NULL;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceCtx* c = nullptr;
+  int st = get_ctx(&c);
+  if (st != GQA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  unsigned v = 0;
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaMemcpy(&v, c->err, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaMemset(c->err, 0, sizeof v)) != cudaSuccess) return cuda_fail(e);
+  if ((v & GQA_DEV_WAIT_TIMEOUT) && c->counters) {
+    // A decode that gave up may have left arrival counters half counted.
+    if ((e = cudaMemset(c->counters, 0, c->counters_cap * sizeof(int))) != cudaSuccess) return cuda_fail(e);
+  }
+  *flags = v;
+  return GQA_OK;
+}
+
+int gqa_decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int* tile_keys, int* num_ctas) {
+  if (!tile_keys || !num_ctas) return GQA_ERR_NULL;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  int sm = 148;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sm = v;
+  } else {
+    cudaGetLastError();
+  }
+  gqa::DecodePlan plan;
+  if (!gqa::decode_plan(B, Hq, Hkv, D, Lmax, sm, &plan)) return GQA_ERR_UNSUPPORTED;
+  *tile_keys = plan.tile_keys;
+  *num_ctas = plan.num_ctas;
+  return GQA_OK;
+}
+
+void gqa_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int cur = -1;
+  bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+  for (size_t d = 0; d < g_dev.size(); ++d) {
+    DeviceCtx& c = g_dev[d];
+    if (!c.ready) continue;
+    cudaSetDevice((int)d);
+    cudaDeviceSynchronize();
+    if (c.ws_part) cudaFree(c.ws_part);
+    if (c.counters) cudaFree(c.counters);
+    if (c.err) cudaFree(c.err);
+    if (c.stage) cudaFree(c.stage);
+    if (c.last_evt) cudaEventDestroy(c.last_evt);
+    c = DeviceCtx();
+  }
+  if (have_cur) cudaSetDevice(cur);
+  cudaGetLastError();
+}
+
+}  // extern "C"

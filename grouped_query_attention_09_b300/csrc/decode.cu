@@ -1,0 +1,589 @@
+// decode.cu -- split-KV GQA decode on sm_103a.
+//
+// One decode step: for every sequence b and query head h, one query vector
+// attends to the first seqlens[b] rows of KV head j = h / G of a bf16
+// [B, Hkv, Lmax, D] cache (G = Hq / Hkv query heads per KV head; the grouping
+// of the GQA paper notes, "分组查询注意力（GQA）", and of the Huawei Cloud post
+// "多头注意力机制的代码实现（MQA和GQA）", section 5).  Decode is bound by reading
+// the KV cache (the paper notes, "QA 相关": the saving of GQA is the smaller
+// cache read from HBM), so the design goal is that every cache byte crosses
+// HBM exactly once and is reused from shared memory by all G query heads of
+// its group -- K/V are never expanded to Hq heads.
+//
+// Work split ("Split-KV": the gsyq.cn page on xformers, "分块计算与内存优化",
+// cuts K/V into blocks computed apart and reduced afterwards):
+//   * the (b, j, key tile) space is flattened pair-major (pair = b*Hkv + j)
+//     and cut into num_ctas contiguous, equal shares; each persistent CTA
+//     streams its share, crossing pair boundaries;
+//   * a pair wholly inside one CTA is normalised and written directly; a pair
+//     cut by a share boundary leaves one partial (running max m, sum l,
+//     unnormalised acc) per piece in a workspace, and the CTA that finishes
+//     the last piece of that pair (an arrival counter) merges the pieces by
+//     log-sum-exp and writes the output -- no second kernel.
+//
+// CTA layout: warps 0..NC-1 consume, warp NC produces.
+//   producer: one lane streams K and V tiles [tile_keys x D] of the cache into
+//     a ring of shared-memory stages with 3-D TMA loads (128-byte swizzle,
+//     evict-first L2 policy), an mbarrier pair per stage;
+//   consumers: a 4 x HS grid of warps; warp (ks, hs) owns keys
+//     [16 ks, 16 ks + 16) of every tile and query heads [8 NT hs, 8 NT (hs+1))
+//     of the group.  Scores are computed transposed, S^T = K q^T, with
+//     mma.sync m16n8k16 (keys in M, heads in N, D in K); the online softmax
+//     runs on the accumulator fragments (per-head max over keys by warp
+//     shuffles); P^T is turned into the B operand of O^T = V^T P^T with
+//     movmatrix; V^T comes from the swizzled V tile through ldmatrix.trans.
+//     The four key-slice states of a head are merged in shared memory at the
+//     end of each piece.
+//   Decode intensity is G flop per cache byte (<= 64), far below the tensor
+//   ridge point, so the warp-level MMA is not the bound; HBM is.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kBN = 64;            // keys per tile
+constexpr int kKW = kBN / 16;      // key-slice warps
+constexpr int kMaxBatch = 1024;    // batches whose tile prefix fits in shared memory
+constexpr int kMaxStages = 8;
+constexpr int kSmemLimit = 232448; // opt-in dynamic shared memory per CTA on sm_100-class parts
+
+struct Params {
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  const int32_t* seqlens;
+  float* part_acc;  // [P][2][G][D]
+  float* part_ml;   // [P][2][2][G]  (m then l; m in log2 units)
+  int* counters;    // [B*Hkv]
+  unsigned* err;
+  int B, Hq, Hkv, G, Lmax;
+  int HS, NC, stages, num_ctas;
+  float scale_log2;
+};
+
+struct SmemLayout {
+  int stage_bytes, k_bytes;
+  int epi_off, red_off, pre_off, bar_off, flag_off, total;
+};
+
+__host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+template <int D>
+__host__ __device__ inline SmemLayout smem_layout(int stages, int Gpad) {
+  SmemLayout s;
+  s.k_bytes = (D / 64) * kBN * 128;
+  s.stage_bytes = 2 * s.k_bytes;
+  s.epi_off = stages * s.stage_bytes;
+  s.red_off = s.epi_off + kKW * Gpad * (D + 4) * 4;
+  s.pre_off = s.red_off + 2 * kKW * Gpad * 4;
+  s.bar_off = round_up(s.pre_off + (kMaxBatch + 1) * 4, 8);
+  s.flag_off = s.bar_off + 2 * stages * 8;
+  s.total = s.flag_off + 4 * (4 + 32) + 1024;  // flags + scan scratch, + slack to align the base
+
+  return s;
+}
+
+// Position in the flattened (b, j, tile) space.
+struct TileIter {
+  int b, j, lt, nb;
+};
+
+__device__ inline void iter_seek(TileIter& it, long long t, const int* pre, int B, int Hkv) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if ((long long)Hkv * pre[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  it.b = lo;
+  it.nb = pre[lo + 1] - pre[lo];
+  long long r = t - (long long)Hkv * pre[lo];
+  it.j = (int)(r / it.nb);
+  it.lt = (int)(r % it.nb);
+}
+
+__device__ inline void iter_next(TileIter& it, const int* pre, int B, int Hkv) {
+  if (++it.lt < it.nb) return;
+  it.lt = 0;
+  if (++it.j < Hkv) return;
+  it.j = 0;
+  do { ++it.b; } while (it.b < B && pre[it.b + 1] == pre[it.b]);
+  it.nb = it.b < B ? pre[it.b + 1] - pre[it.b] : 0;
+}
+
+// CTA whose share [floor(c T / P), floor((c+1) T / P)) holds tile t.
+__device__ inline int cta_of(long long t, long long T, int P) {
+  return (int)(((t + 1) * P + T - 1) / T) - 1;
+}
+
+__device__ inline int clamp_len(int len, int Lmax) { return len < 0 ? 0 : (len > Lmax ? Lmax : len); }
+
+template <int D, int NT>
+__global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const Params p) {
+  constexpr int KT = D / 16;  // 16-wide k-steps over D (QK) and m-tiles over D (PV)
+  const int Gpad = p.HS * 8 * NT;
+  const SmemLayout L = smem_layout<D>(p.stages, Gpad);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* epi = reinterpret_cast<float*>(smem + L.epi_off);          // [KW][Gpad][D+4]
+  float* red_m = reinterpret_cast<float*>(smem + L.red_off);        // [KW][Gpad]
+  float* red_l = red_m + kKW * Gpad;                                 // [KW][Gpad]
+  int* pre = reinterpret_cast<int*>(smem + L.pre_off);               // [B+1]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* empty = full + p.stages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag_off);
+  volatile int* last_flag = abort_flag + 1;
+  volatile int* chi_flag = abort_flag + 2;
+  int* warp_tot = reinterpret_cast<int*>(smem + L.flag_off) + 4;  // [32]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NC = p.NC, nthr = blockDim.x;
+  const int B = p.B, Hkv = p.Hkv, G = p.G;
+
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NC);
+    }
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == NC && lane == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+
+  // ---- tile count per batch and its exclusive prefix pre[0..B] (block scan)
+  {
+    const int per = (B + nthr - 1) / nthr;
+    const int lo = tid * per, hi = min(B, lo + per);
+    int local = 0;
+    unsigned flags = 0;
+    for (int i = lo; i < hi; ++i) {
+      int len = p.seqlens[i];
+      if (len > p.Lmax) flags |= GQA_DEV_SEQLEN_CLAMPED;
+      if (len <= 0) flags |= GQA_DEV_EMPTY_CONTEXT;
+      local += (clamp_len(len, p.Lmax) + kBN - 1) / kBN;
+    }
+    if (flags && blockIdx.x == 0) atomicOr(p.err, flags);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = nthr >> 5;
+      int w = lane < nw ? warp_tot[lane] : 0;
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += v;
+      }
+      if (lane < nw) warp_tot[lane] = wi - w;  // exclusive warp offsets
+    }
+    __syncthreads();
+    int run = warp_tot[warp] + incl - local;
+    for (int i = lo; i < hi; ++i) {
+      pre[i] = run;
+      run += (clamp_len(p.seqlens[i], p.Lmax) + kBN - 1) / kBN;
+    }
+    if (lo < B && hi == B) pre[B] = run;
+  }
+  __syncthreads();
+
+  // Shares: the first P = min(CTAs, tiles) CTAs each take a non-empty,
+  // contiguous share [s_c, e_c) of the T tiles; the others only zero-fill.
+  const long long T = (long long)Hkv * pre[B];
+  const int P = (int)(T < p.num_ctas ? T : p.num_ctas);
+  const bool active = (int)blockIdx.x < P;
+  const long long s_c = active ? T * blockIdx.x / P : 0;
+  const long long e_c = active ? T * (blockIdx.x + 1) / P : 0;
+
+  if (warp == NC) {
+    // ============================== producer ==============================
+    if (lane == 0 && s_c < e_c) {
+      const uint64_t pol = l2_policy_evict_first();
+      TileIter it;
+      iter_seek(it, s_c, pre, B, Hkv);
+      long long issued = 0;
+      for (long long t = s_c; t < e_c; ++t) {
+        const int i = (int)(t - s_c);
+        const int s = i % p.stages;
+        if (i >= p.stages) {
+          if (!mbar_wait_bounded(&empty[s], ((i / p.stages) & 1) ^ 1, abort_flag, p.err)) break;
+        }
+        uint8_t* kdst = smem + s * L.stage_bytes;
+        uint8_t* vdst = kdst + L.k_bytes;
+        mbar_arrive_expect_tx(&full[s], L.stage_bytes);
+        const int z = it.b * Hkv + it.j, y = it.lt * kBN;
+#pragma unroll
+        for (int box = 0; box < D / 64; ++box) {
+          tma_load_3d(kdst + box * kBN * 128, &tmK, box * 64, y, z, &full[s], pol);
+          tma_load_3d(vdst + box * kBN * 128, &tmV, box * 64, y, z, &full[s], pol);
+        }
+        issued = i + 1;
+        iter_next(it, pre, B, Hkv);
+      }
+      // Wait (bounded) until every copy this thread issued has landed.
+      const long long first = issued > p.stages ? issued - p.stages : 0;
+      for (long long i = first; i < issued; ++i) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (!mbar_try_wait(&full[i % p.stages], (uint32_t)((i / p.stages) & 1))) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(p.err, GQA_DEV_WAIT_TIMEOUT);
+            break;
+          }
+        }
+      }
+    }
+  } else {
+    // ============================== consumers =============================
+    const int ks = warp % kKW;  // key slice
+    const int hs = warp / kKW;  // head slice
+    const int key0 = ks * 16;
+    const int cthreads = NC * 32;
+
+    // Zero output rows of sequences with an empty context (this CTA's share).
+    for (int b = blockIdx.x; b < B; b += p.num_ctas) {
+      if (pre[b + 1] != pre[b]) continue;
+      __nv_bfloat16* o = p.out + (size_t)b * p.Hq * D;
+      for (int e = tid; e < p.Hq * D; e += cthreads) o[e] = __float2bfloat16_rn(0.f);
+    }
+
+    // Per-lane constants of the ldmatrix addressing (128-byte swizzle: the
+    // 16-byte chunk c of row r sits at chunk c ^ (r & 7)).
+    const int sw = lane & 7;
+    const int k_row = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;  // K: M0..M3 = (k0-7,c),(k8-15,c),(k0-7,c+1),(k8-15,c+1)
+    const int k_chunk_add = lane >> 4;
+    const int v_row = key0 + (lane & 7) + (lane >> 4) * 8;        // V^T: (k0-7,c),(k0-7,c+1),(k8-15,c),(k8-15,c+1)
+    const int v_chunk_add = (lane >> 3) & 1;
+
+    float acc[KT][NT][4];
+    float m_run[NT][2], l_run[NT][2];
+    uint32_t qf[KT][NT][2];
+    int seg_lt0 = 0, len_b = 0;
+    bool live = true;
+
+    TileIter it;
+    if (s_c < e_c) iter_seek(it, s_c, pre, B, Hkv);
+    for (long long t = s_c; t < e_c; ++t) {
+      const int i = (int)(t - s_c);
+      const int s = i % p.stages;
+      const bool seg_first = (t == s_c) || (it.lt == 0);
+      const bool seg_last = (t == e_c - 1) || (it.lt == it.nb - 1);
+      const int pair = it.b * Hkv + it.j;
+
+      if (seg_first) {
+        seg_lt0 = it.lt;
+        len_b = clamp_len(p.seqlens[it.b], p.Lmax);
+        const __nv_bfloat16* qb = p.q + ((size_t)it.b * p.Hq + (size_t)it.j * G) * D;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int hg = (hs * NT + nt) * 8 + (lane >> 2);
+#pragma unroll
+          for (int kk = 0; kk < KT; ++kk) {
+            if (hg < G) {
+              const uint32_t* qp = reinterpret_cast<const uint32_t*>(qb + (size_t)hg * D + kk * 16 + 2 * (lane & 3));
+              qf[kk][nt][0] = __ldg(qp);
+              qf[kk][nt][1] = __ldg(qp + 4);
+            } else {
+              qf[kk][nt][0] = 0u;
+              qf[kk][nt][1] = 0u;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            m_run[nt][e] = -INFINITY;
+            l_run[nt][e] = 0.f;
+          }
+#pragma unroll
+          for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[kk][nt][e] = 0.f;
+        }
+      }
+
+      if (live) live = mbar_wait_bounded(&full[s], (uint32_t)((i / p.stages) & 1), abort_flag, p.err);
+      if (live) {
+        const uint32_t kbase = smem_u32(smem + s * L.stage_bytes);
+        const uint32_t vbase = kbase + L.k_bytes;
+        const int valid = min(kBN, len_b - it.lt * kBN);  // >= 1
+
+        if (valid < key0 + 16) {
+          // Rows past the sequence end hold whatever the cache holds there
+          // (possibly NaN); zero this warp's V rows so P = 0 stays 0.
+          const int r0 = max(valid, key0);
+          const int nrows = key0 + 16 - r0;
+          uint8_t* vtile = smem + s * L.stage_bytes + L.k_bytes;
+          for (int e = lane; e < nrows * (D / 64) * 8; e += 32) {
+            const int row = r0 + e / ((D / 64) * 8);
+            const int rem = e % ((D / 64) * 8);
+            const int box = rem / 8, chunk = rem % 8;
+            *reinterpret_cast<uint4*>(vtile + box * kBN * 128 + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+
+        // ---- S^T = K q^T over this warp's 16 keys
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+          uint32_t a[4];
+          const int chunk = (kk & 3) * 2 + k_chunk_add;
+          ldmatrix_x4(a, kbase + (kk >> 2) * kBN * 128 + k_row * 128 + ((chunk ^ sw) << 4));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], a, qf[kk][nt][0], qf[kk][nt][1]);
+        }
+
+        // ---- online softmax (log2 domain); rows = keys, columns = heads
+        const bool v_lo = key0 + (lane >> 2) < valid;
+        const bool v_hi = key0 + (lane >> 2) + 8 < valid;
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float x[4];
+          x[0] = v_lo ? sc[nt][0] * p.scale_log2 : -INFINITY;
+          x[1] = v_lo ? sc[nt][1] * p.scale_log2 : -INFINITY;
+          x[2] = v_hi ? sc[nt][2] * p.scale_log2 : -INFINITY;
+          x[3] = v_hi ? sc[nt][3] * p.scale_log2 : -INFINITY;
+          float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+          }
+          const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+          const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+          const float al0 = fast_exp2(m_run[nt][0] - mu0), al1 = fast_exp2(m_run[nt][1] - mu1);
+          m_run[nt][0] = mn0;
+          m_run[nt][1] = mn1;
+          const float p0 = fast_exp2(x[0] - mu0), p1 = fast_exp2(x[1] - mu1);
+          const float p2 = fast_exp2(x[2] - mu0), p3 = fast_exp2(x[3] - mu1);
+          l_run[nt][0] = l_run[nt][0] * al0 + (p0 + p2);
+          l_run[nt][1] = l_run[nt][1] * al1 + (p1 + p3);
+#pragma unroll
+          for (int kk = 0; kk < KT; ++kk) {
+            acc[kk][nt][0] *= al0;
+            acc[kk][nt][1] *= al1;
+            acc[kk][nt][2] *= al0;
+            acc[kk][nt][3] *= al1;
+          }
+          pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
+          pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+        }
+
+        // ---- O^T += V^T P^T
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+          uint32_t a[4];
+          const int chunk = (mt & 3) * 2 + v_chunk_add;
+          ldmatrix_x4_trans(a, vbase + (mt >> 2) * kBN * 128 + v_row * 128 + ((chunk ^ sw) << 4));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a, pb[nt][0], pb[nt][1]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+
+      if (seg_last) {
+        // ---- merge the key-slice states of this piece, then output or partial
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float l = l_run[nt][e];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            const int hg = (hs * NT + nt) * 8 + 2 * (lane & 3) + e;
+            if ((lane >> 2) == 0) {
+              red_m[ks * Gpad + hg] = m_run[nt][e];
+              red_l[ks * Gpad + hg] = l;
+            }
+          }
+#pragma unroll
+          for (int mt = 0; mt < KT; ++mt) {
+            const int d = mt * 16 + (lane >> 2);
+            const int hg = (hs * NT + nt) * 8 + 2 * (lane & 3);
+            float* e0 = epi + (size_t)(ks * Gpad + hg) * (D + 4);
+            float* e1 = e0 + (D + 4);
+            e0[d] = acc[mt][nt][0];
+            e1[d] = acc[mt][nt][1];
+            e0[d + 8] = acc[mt][nt][2];
+            e1[d + 8] = acc[mt][nt][3];
+          }
+        }
+        named_bar_sync(1, cthreads);
+
+        const bool complete = (seg_lt0 == 0) && (it.lt == it.nb - 1);
+        const int slot = seg_lt0 == 0 ? 1 : 0;
+        const size_t slot_idx = (size_t)blockIdx.x * 2 + slot;
+        __nv_bfloat16* outp = p.out + ((size_t)it.b * p.Hq + (size_t)it.j * G) * D;
+        for (int e = tid; e < G * (D / 2); e += cthreads) {
+          const int h = e / (D / 2), d = 2 * (e % (D / 2));
+          float M = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < kKW; ++k) M = fmaxf(M, red_m[k * Gpad + h]);
+          const float Mu = M == -INFINITY ? 0.f : M;
+          float Ls = 0.f, s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int k = 0; k < kKW; ++k) {
+            const float f = fast_exp2(red_m[k * Gpad + h] - Mu);
+            const float* ep = epi + (size_t)(k * Gpad + h) * (D + 4) + d;
+            Ls += f * red_l[k * Gpad + h];
+            s0 += f * ep[0];
+            s1 += f * ep[1];
+          }
+          if (complete) {
+            const float inv = 1.f / Ls;
+            *reinterpret_cast<__nv_bfloat162*>(outp + (size_t)h * D + d) = __floats2bfloat162_rn(s0 * inv, s1 * inv);
+          } else {
+            float* pa = p.part_acc + (slot_idx * G + h) * D + d;
+            pa[0] = s0;
+            pa[1] = s1;
+            if (d == 0) {
+              p.part_ml[(slot_idx * 2 + 0) * G + h] = M;
+              p.part_ml[(slot_idx * 2 + 1) * G + h] = Ls;
+            }
+          }
+        }
+
+        if (!complete) {
+          __threadfence();
+          named_bar_sync(1, cthreads);
+          if (tid == 0) {
+            const long long o_p = (long long)Hkv * pre[it.b] + (long long)it.j * it.nb;
+            const int c_lo = cta_of(o_p, T, P);
+            const int c_hi = cta_of(o_p + it.nb - 1, T, P);
+            const int old = atomicAdd(&p.counters[pair], 1);
+            const bool last = old == c_hi - c_lo;
+            if (last) p.counters[pair] = 0;  // ready for the next call
+            *last_flag = last ? (c_lo + 1) : 0;  // encodes c_lo
+            *chi_flag = c_hi;
+          }
+          named_bar_sync(1, cthreads);
+          const int lf = *last_flag;
+          if (lf) {
+            __threadfence();
+            const int c_lo = lf - 1, c_hi = *chi_flag;
+            for (int e = tid; e < G * (D / 2); e += cthreads) {
+              const int h = e / (D / 2), d = 2 * (e % (D / 2));
+              float M = -INFINITY;
+              for (int c = c_lo; c <= c_hi; ++c) {
+                const size_t si = (size_t)c * 2 + (c == c_lo ? 1 : 0);
+                M = fmaxf(M, __ldcg(p.part_ml + (si * 2 + 0) * G + h));
+              }
+              const float Mu = M == -INFINITY ? 0.f : M;
+              float Ls = 0.f, s0 = 0.f, s1 = 0.f;
+              for (int c = c_lo; c <= c_hi; ++c) {
+                const size_t si = (size_t)c * 2 + (c == c_lo ? 1 : 0);
+                const float f = fast_exp2(__ldcg(p.part_ml + (si * 2 + 0) * G + h) - Mu);
+                Ls += f * __ldcg(p.part_ml + (si * 2 + 1) * G + h);
+                const float2 a2 = __ldcg(reinterpret_cast<const float2*>(p.part_acc + (si * G + h) * D + d));
+                s0 += f * a2.x;
+                s1 += f * a2.y;
+              }
+              const float inv = 1.f / Ls;
+              *reinterpret_cast<__nv_bfloat162*>(outp + (size_t)h * D + d) = __floats2bfloat162_rn(s0 * inv, s1 * inv);
+            }
+          }
+        }
+        named_bar_sync(1, cthreads);
+      }
+      iter_next(it, pre, B, Hkv);
+    }
+  }
+  __syncthreads();
+}
+
+template <int D, int NT>
+cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream) {
+  CUtensorMap tmK, tmV;
+  const uint64_t pairs = (uint64_t)a.B * a.Hkv;
+  const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)a.Lmax * D * 2;
+  if (encode_tmap_bf16_3d(&tmK, a.k_cache, D, a.Lmax, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS ||
+      encode_tmap_bf16_3d(&tmV, a.v_cache, D, a.Lmax, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  Params p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.seqlens = a.seqlens;
+  p.part_acc = a.ws_part;
+  p.part_ml = a.ws_part + (size_t)plan.num_ctas * 2 * plan.G * D;
+  p.counters = a.ws_counters;
+  p.err = a.err;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = plan.G;
+  p.Lmax = a.Lmax;
+  p.HS = plan.HS;
+  p.NC = kKW * plan.HS;
+  p.stages = plan.stages;
+  p.num_ctas = plan.num_ctas;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  auto kern = decode_kernel<D, NT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem_bytes);
+  if (e != cudaSuccess) return e;
+  kern<<<plan.num_ctas, plan.threads, plan.smem_bytes, stream>>>(tmK, tmV, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan) {
+  if (B < 1 || B > kMaxBatch || Hkv < 1 || Hq % Hkv != 0 || Lmax < 1) return false;
+  if (D != 64 && D != 128) return false;
+  const int G = Hq / Hkv;
+  int Gpad, NT, HS;
+  if (G <= 8) {
+    Gpad = 8; NT = 1; HS = 1;
+  } else if (G == 16 || G == 32) {
+    Gpad = G; NT = 2; HS = G / 16;
+  } else {
+    return false;
+  }
+  plan->D = D;
+  plan->G = G;
+  plan->Gpad = Gpad;
+  plan->NT = NT;
+  plan->HS = HS;
+  plan->tile_keys = kBN;
+  plan->threads = 32 * (kKW * HS + 1);
+  const long long tiles_max = (long long)B * Hkv * ((Lmax + kBN - 1) / kBN);
+  plan->num_ctas = (int)std::min<long long>(tiles_max, std::max(1, sm_count));
+  SmemLayout l0 = D == 64 ? smem_layout<64>(0, Gpad) : smem_layout<128>(0, Gpad);
+  const int stages = std::min(kMaxStages, (kSmemLimit - l0.total - 2 * kMaxStages * 8) / l0.stage_bytes);
+  if (stages < 2) return false;
+  plan->stages = stages;
+  plan->smem_bytes = (size_t)(D == 64 ? smem_layout<64>(stages, Gpad) : smem_layout<128>(stages, Gpad)).total;
+  plan->ws_part_floats = (size_t)plan->num_ctas * 2 * G * (D + 2);
+  plan->ws_counters = (size_t)B * Hkv;
+  return true;
+}
+
+cudaError_t decode_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream) {
+  if (plan.D == 128) {
+    return plan.NT == 1 ? launch_t<128, 1>(plan, a, stream) : launch_t<128, 2>(plan, a, stream);
+  }
+  return plan.NT == 1 ? launch_t<64, 1>(plan, a, stream) : launch_t<64, 2>(plan, a, stream);
+}
+
+}  // namespace gqa

@@ -1,0 +1,60 @@
+// internal.h -- host-side declarations shared by the translation units of libgqa.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gqa {
+
+// Encodes a 3-D bf16 tiled tensor map (dims innermost first, strides in bytes
+// for dims 1 and 2) with 128-byte swizzle and zero fill outside the tensor.
+CUresult encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1,
+                             uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
+                             uint32_t box1, uint32_t box2);
+
+// ------------------------------------------------------------------ decode
+struct DecodePlan {
+  int D, G, Gpad, NT, HS;  // head dim, group size, padded group, n-tiles/warp, head slices
+  int tile_keys;           // keys per pipeline tile
+  int num_ctas;            // persistent CTAs
+  int threads;             // threads per CTA
+  int stages;              // pipeline depth
+  size_t smem_bytes;       // dynamic shared memory per CTA
+  size_t ws_part_floats;   // partial-result floats (acc + m + l)
+  size_t ws_counters;      // per-(b, kv head) arrival counters
+};
+
+// Chooses tile size, persistent grid and pipeline depth; returns false if the
+// shape is not supported by the decode kernels.
+bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan);
+
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* seqlens;
+  void* out;
+  int B, Hq, Hkv, D, Lmax;
+  float scale;
+  float* ws_part;     // >= plan.ws_part_floats floats
+  int* ws_counters;   // >= plan.ws_counters ints, zero on entry, zero on exit
+  unsigned* err;      // device status word
+};
+
+cudaError_t decode_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream);
+
+// ------------------------------------------------------------------ prefill
+struct PrefillArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  int B, L, Hq, Hkv, D, causal;
+  unsigned* err;
+};
+
+bool prefill_supported(int D);
+cudaError_t prefill_launch(const PrefillArgs& a, int sm_count, cudaStream_t stream);
+
+}  // namespace gqa

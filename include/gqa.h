@@ -1,0 +1,155 @@
+/*
+ * gqa.h -- C ABI of libgqa.so, a single-GPU grouped-query attention (GQA)
+ * engine for NVIDIA B300 (sm_103a).
+ *
+ * Grouped-query attention: Hq query heads are split into Hkv groups; every
+ * group shares one K head and one V head, and query head h reads KV head
+ * h / (Hq / Hkv) (the GQA paper notes on 51969.com, section "分组查询注意力
+ * （GQA）"; the grouping `head_index // n_head_per_group` of the Huawei Cloud
+ * post "多头注意力机制的代码实现（MQA和GQA）", section 5; the
+ * `repeat_interleave` of "手把手教你用PyTorch实现GQA", section 1.3).
+ * Hkv == Hq is multi-head attention and Hkv == 1 is multi-query attention.
+ * Per head, out = softmax(scale * q K^T) V (Huawei Cloud post, section 5 code:
+ * Q @ K^T, divide by sqrt(head_size), softmax, @ V).
+ *
+ * Conventions for every entry point
+ *   - Tensors are dense, row-major, bf16 unless stated; pointers are DEVICE
+ *     pointers of the current CUDA device unless the name says "host", and
+ *     must be 16-byte aligned.  The caller allocates and owns every tensor and
+ *     the stream; the library only borrows the pointers until the enqueued
+ *     work has run.  K/V are never expanded to Hq heads in memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device entry points are asynchronous: they enqueue kernels on
+ *     `stream` and return without synchronising.
+ *   - Every function returns a gqa_status (0 = GQA_OK).  Argument errors are
+ *     detected on the host before anything is enqueued; nothing traps.
+ *   - Conditions seen on the device (a sequence length above the cache
+ *     capacity, an empty context, a bounded wait that gave up) never trap:
+ *     the kernel takes the documented fallback and sets a bit in a per-device
+ *     status word that gqa_get_device_status() returns.
+ *   - Thread safety: calls may come from several host threads; the library
+ *     serialises access to its per-device workspace.  Two decode calls that
+ *     share the workspace must not run concurrently on different streams; the
+ *     library orders them on the stream of the later call.
+ */
+#ifndef GQA_H_
+#define GQA_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GQA_API __attribute__((visibility("default")))
+#else
+#define GQA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gqa_status {
+  GQA_OK = 0,
+  GQA_ERR_INVALID_ARG = 1, /* a size <= 0, Hq % Hkv != 0, causal not 0/1, bad scale */
+  GQA_ERR_UNSUPPORTED = 2, /* a shape the kernels do not implement (see each call) */
+  GQA_ERR_NULL = 3,        /* a required pointer is NULL */
+  GQA_ERR_MISALIGNED = 4,  /* a tensor pointer is not 16-byte aligned */
+  GQA_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed; see gqa_status_string */
+  GQA_ERR_NO_DEVICE = 6    /* no usable sm_103 device, or the kernels are not loadable */
+} gqa_status;
+
+/* Bits of the per-device status word (gqa_get_device_status). */
+#define GQA_DEV_SEQLEN_CLAMPED 0x1u /* some seqlens[b] > Lmax; Lmax keys were used */
+#define GQA_DEV_EMPTY_CONTEXT 0x2u  /* some seqlens[b] <= 0; that row of out is zero */
+#define GQA_DEV_WAIT_TIMEOUT 0x4u   /* a pipeline wait gave up; results are invalid */
+
+/*
+ * gqa_decode -- one decode step: every sequence b has one new query token per
+ * query head, attending to the first seqlens[b] cached keys of its group.
+ *
+ *   q        [B, Hq, D]          bf16, device
+ *   k_cache  [B, Hkv, Lmax, D]   bf16, device; row t of (b, j) at element
+ *   v_cache  [B, Hkv, Lmax, D]     offset ((b*Hkv + j)*Lmax + t)*D
+ *   seqlens  [B]                 int32, device; keys visible to sequence b
+ *                                (the new token's own K/V already appended).
+ *                                Read only on the device: no host sync.
+ *   out      [B, Hq, D]          bf16, device, written (RNE from fp32)
+ *   scale    logit scale, finite and > 0 (usually 1/sqrt(D))
+ *
+ * There is no mask inside [0, seqlens[b]); cache rows at or beyond seqlens[b]
+ * are never read into the result (they may hold anything, NaN included).
+ * seqlens[b] > Lmax is clamped to Lmax; seqlens[b] <= 0 gives a zero output
+ * row; both set a device status bit.
+ *
+ * Supported: D in {64, 128}; G = Hq/Hkv in {1..8, 16, 32};
+ * 1 <= B <= 1024.  Otherwise GQA_ERR_UNSUPPORTED.
+ *
+ * Work is split across a persistent grid: the (b, j, key-tile) space is cut
+ * into equal contiguous shares, one per CTA (split-KV, the gsyq.cn page on
+ * xformers, "分块计算与内存优化"), and the pieces of a (b, j) that landed in
+ * different CTAs are merged by log-sum-exp in the same launch.  The partial
+ * results live in a library-owned device workspace that is allocated on the
+ * first call on a device (and grown when a later call needs more), kept until
+ * gqa_release(); this first call allocates and so must not be made during
+ * stream capture.
+ */
+GQA_API int gqa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens,
+               void* out, int B, int Hq, int Hkv, int D, int Lmax, float scale, void* stream);
+
+/*
+ * gqa_prefill -- attention of L query tokens over the same L keys (prompt
+ * processing), causal or not.
+ *
+ *   q, out   [B, Hq, L, D]   bf16, device
+ *   k, v     [B, Hkv, L, D]  bf16, device
+ *   causal   1: query i sees keys t <= i (the square mask triu(ones, 1) ->
+ *               -inf of the Huawei Cloud post, section 5, applied);
+ *            0: every query sees all L keys.
+ *   scale    fixed at 1/sqrt(D) (the post divides by head_size ** 0.5).
+ *
+ * QK^T and PV are dense bf16 contractions on the tcgen05 tensor cores with
+ * fp32 accumulators in tensor memory; the softmax is fp32; P is rounded to
+ * bf16 before PV; out is rounded RNE.
+ *
+ * Supported: D == 128, any L >= 1, any G.  Otherwise GQA_ERR_UNSUPPORTED.
+ * Needs no workspace and allocates nothing.
+ */
+GQA_API int gqa_prefill(const void* q, const void* k, const void* v, void* out, int B, int L, int Hq,
+                int Hkv, int D, int causal, void* stream);
+
+/*
+ * gqa_decode_host / gqa_prefill_host -- the same computations on HOST
+ * buffers (pageable or pinned).  The call copies the inputs to library-owned
+ * device buffers on `stream`, runs the device entry point, copies `out` back
+ * and synchronises `stream` before returning, so the host output is ready.
+ * Shapes, layouts and errors are those of the device calls; seqlens_host is
+ * host memory here.  The staging buffers are kept (and grown) until
+ * gqa_release().
+ */
+GQA_API int gqa_decode_host(const void* q_host, const void* k_cache_host, const void* v_cache_host,
+                    const int32_t* seqlens_host, void* out_host, int B, int Hq, int Hkv, int D,
+                    int Lmax, float scale, void* stream);
+GQA_API int gqa_prefill_host(const void* q_host, const void* k_host, const void* v_host, void* out_host,
+                     int B, int L, int Hq, int Hkv, int D, int causal, void* stream);
+
+/* Human-readable text of a status (for GQA_ERR_CUDA it names the CUDA error
+ * of the last failure on this host thread).  Never NULL. */
+GQA_API const char* gqa_status_string(int status);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word (GQA_DEV_* bits) into *flags.  Returns GQA_OK or GQA_ERR_CUDA. */
+GQA_API int gqa_get_device_status(void* stream, uint32_t* flags);
+
+/* Number of key tiles of the decode split and persistent CTAs the next
+ * gqa_decode with these sizes would use, for tests and tuning:
+ * *tile_keys, *num_ctas.  Returns GQA_OK or an argument error. */
+GQA_API int gqa_decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int* tile_keys, int* num_ctas);
+
+/* Frees every device buffer the library holds on every device it touched.
+ * No call may be in flight.  Safe to call more than once. */
+GQA_API void gqa_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_H_ */

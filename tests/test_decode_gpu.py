@@ -1,0 +1,156 @@
+"""Decode parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bar (written here, applied element-wise): |gpu - oracle| <= 1e-2 + 1e-2 |oracle|
+on the same seeded bf16 inputs.  The kernel accumulates in fp32, rounds the
+softmax weights to bf16 before P V and rounds the output to bf16; at |out|
+<= ~4 the bf16 output rounding alone is up to 2^-9 |out|, well inside the bar.
+"""
+import numpy as np
+import pytest
+import torch
+
+from grouped_query_attention_09_b300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+RTOL = 1e-2
+
+
+def assert_parity(gpu, ref, what=""):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert gpu.shape == ref.shape
+    assert np.isfinite(gpu).all(), f"{what}: non-finite output"
+    err = np.abs(gpu - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    if bad.any():
+        idx = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; worst at {idx}: "
+                             f"gpu={gpu[idx]!r} oracle={ref[idx]!r}")
+
+
+def run_decode(g, q, k, v, sl, scale, dev, stream=None):
+    qd, kd, vd, sld = q.to(dev), k.to(dev), v.to(dev), sl.to(dev)
+    out = g.gqa_decode(qd, kd, vd, sld, scale=scale, stream=stream)
+    flags = g.gqa_get_device_status(stream=stream)
+    return out.double().cpu().numpy(), flags
+
+
+def oracle_decode(oracle_mod, q, k, v, sl, scale, check=True):
+    return oracle_mod.decode(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), sl.numpy(), scale, check=check)
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b", "llama2_70b", "mqa"])
+def test_workload_parity_full(gqa_lib, oracle_mod, cuda_device, name):
+    """Every output element of the four decode workloads at full size, in the
+    launch configuration the benchmark times."""
+    w = W.WORKLOADS[name]
+    q, k, v, sl = W.make_decode_inputs(w)
+    out, flags = run_decode(gqa_lib, q, k, v, sl, w.scale, cuda_device)
+    assert flags == 0
+    assert_parity(out, oracle_decode(oracle_mod, q, k, v, sl, w.scale), name)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,Lmax,lens", [
+    (3, 8, 2, 128, 700, [700, 333, 65]),      # ragged tails, many tiles, every pair split
+    (2, 8, 2, 64, 128, [1, 128]),             # single key; exactly two tiles
+    (4, 4, 4, 128, 257, [63, 64, 65, 257]),   # MHA endpoint; tile boundaries
+    (5, 16, 1, 128, 300, [300, 1, 150, 64, 129]),  # MQA endpoint G = 16
+    (2, 32, 1, 64, 1000, [999, 1000]),        # G = 32 (two head slices) at D = 64
+    (2, 6, 2, 64, 96, [96, 17]),              # G = 3 (padded heads)
+    (1, 1, 1, 128, 5000, [4999]),             # one head, long
+    (2, 16, 2, 128, 640, [640, 600]),         # G = 8
+])
+def test_shapes_parity(gqa_lib, oracle_mod, cuda_device, B, Hq, Hkv, D, Lmax, lens):
+    w = W.DecodeWorkload("case", B, Hq, Hkv, D, Lmax, 1, Lmax, 1000 + B * Hq + D + Lmax)
+    q, k, v, _ = W.make_decode_inputs(w)
+    sl = torch.tensor(lens, dtype=torch.int32)
+    out, flags = run_decode(gqa_lib, q, k, v, sl, w.scale, cuda_device)
+    assert flags == 0
+    assert_parity(out, oracle_decode(oracle_mod, q, k, v, sl, w.scale), f"{B},{Hq},{Hkv},{D},{lens}")
+
+
+def test_many_short_sequences_complete_in_one_cta(gqa_lib, oracle_mod, cuda_device):
+    """Short sequences in a big batch: most (b, kv head) pairs fall inside one
+    CTA's share and take the direct-output path rather than the merge."""
+    w = W.DecodeWorkload("short", 512, 8, 2, 64, 200, 1, 200, 77)
+    q, k, v, sl = W.make_decode_inputs(w)
+    out, flags = run_decode(gqa_lib, q, k, v, sl, w.scale, cuda_device)
+    assert flags == 0
+    assert_parity(out, oracle_decode(oracle_mod, q, k, v, sl, w.scale), "short")
+
+
+def test_nan_tail_is_never_read(gqa_lib, oracle_mod, cuda_device):
+    """Cache rows past seqlens[b] filled with NaN (the poison test): the kernel
+    must neither read them into a score nor let 0 * NaN into P V."""
+    w = W.DecodeWorkload("poison", 4, 16, 4, 128, 1024, 1, 1024, 31)
+    q, k, v, _ = W.make_decode_inputs(w)
+    sl = torch.tensor([1024, 1, 700, 65], dtype=torch.int32)
+    W.poison_tail(k, v, sl)
+    out, flags = run_decode(gqa_lib, q, k, v, sl, w.scale, cuda_device)
+    assert flags == 0
+    assert_parity(out, oracle_decode(oracle_mod, q, k, v, sl, w.scale), "nan tail")
+
+
+def test_peaky_softmax(gqa_lib, oracle_mod, cuda_device):
+    """q scaled x8 makes the softmax sharp, so weight errors are not hidden by
+    near-uniform attention."""
+    w = W.DecodeWorkload("peaky", 4, 32, 8, 128, 2048, 100, 2048, 41)
+    q, k, v, sl = W.make_decode_inputs(w, q_mult=8.0)
+    out, flags = run_decode(gqa_lib, q, k, v, sl, w.scale, cuda_device)
+    assert flags == 0
+    assert_parity(out, oracle_decode(oracle_mod, q, k, v, sl, w.scale), "peaky")
+
+
+def test_scale_argument(gqa_lib, oracle_mod, cuda_device):
+    w = W.DecodeWorkload("scale", 2, 8, 2, 128, 300, 1, 300, 51)
+    q, k, v, sl = W.make_decode_inputs(w)
+    for scale in (0.02, 0.3):
+        out, flags = run_decode(gqa_lib, q, k, v, sl, scale, cuda_device)
+        assert_parity(out, oracle_decode(oracle_mod, q, k, v, sl, scale), f"scale {scale}")
+
+
+def test_empty_and_clamped_lengths_are_flagged(gqa_lib, oracle_mod, cuda_device):
+    """seqlens[b] <= 0 -> zero row + GQA_DEV_EMPTY_CONTEXT; seqlens[b] > Lmax ->
+    Lmax keys + GQA_DEV_SEQLEN_CLAMPED; the other rows are unaffected."""
+    w = W.DecodeWorkload("edge", 4, 8, 2, 128, 256, 1, 256, 61)
+    q, k, v, _ = W.make_decode_inputs(w)
+    sl = torch.tensor([0, 256, 9999, -5], dtype=torch.int32)
+    out, flags = run_decode(gqa_lib, q, k, v, sl, w.scale, cuda_device)
+    assert flags == (gqa_lib.GQA_DEV_EMPTY_CONTEXT | gqa_lib.GQA_DEV_SEQLEN_CLAMPED)
+    assert np.all(out[0] == 0) and np.all(out[3] == 0)
+    ref = oracle_decode(oracle_mod, q, k, v, torch.tensor([1, 256, 256, 1], dtype=torch.int32), w.scale)
+    assert_parity(out[1:3], ref[1:3], "clamped")
+    assert gqa_lib.gqa_get_device_status() == 0  # read-and-clear
+
+
+def test_repeatable_and_counters_reset(gqa_lib, cuda_device):
+    """Two identical calls give identical bits: the arrival counters of the
+    in-kernel merge are back at zero after every call."""
+    w = W.WORKLOADS["mqa"]
+    q, k, v, sl = [t.to(cuda_device) for t in W.make_decode_inputs(w)]
+    a = gqa_lib.gqa_decode(q, k, v, sl).clone()
+    for _ in range(3):
+        b = gqa_lib.gqa_decode(q, k, v, sl)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert gqa_lib.gqa_get_device_status() == 0
+
+
+def test_side_stream_and_host_entry_point(gqa_lib, cuda_device):
+    """A non-default stream gives the same bits; gqa_decode_host on host
+    buffers gives the same bits as gqa_decode on device buffers."""
+    w = W.WORKLOADS["tiny"]
+    q, k, v, sl = W.make_decode_inputs(w)
+    ref = gqa_lib.gqa_decode(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device), sl.to(cuda_device))
+    s = torch.cuda.Stream(cuda_device)
+    with torch.cuda.stream(s):
+        qd, kd, vd, sld = q.to(cuda_device), k.to(cuda_device), v.to(cuda_device), sl.to(cuda_device)
+        other = gqa_lib.gqa_decode(qd, kd, vd, sld, stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(ref, other)
+    host = gqa_lib.gqa_decode_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), sl.pin_memory())
+    assert torch.equal(ref.cpu(), host)
