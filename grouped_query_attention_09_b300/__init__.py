@@ -24,13 +24,15 @@ GQA_ERR_NULL = 3
 GQA_ERR_MISALIGNED = 4
 GQA_ERR_CUDA = 5
 GQA_ERR_NO_DEVICE = 6
+GQA_ERR_TOO_LARGE = 7
 
 GQA_DEV_SEQLEN_CLAMPED = 0x1
 GQA_DEV_EMPTY_CONTEXT = 0x2
 GQA_DEV_WAIT_TIMEOUT = 0x4
 
 EXPORTED = ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host",
-            "gqa_status_string", "gqa_get_device_status", "gqa_decode_plan", "gqa_release")
+            "gqa_status_string", "gqa_get_device_status", "gqa_decode_plan", "gqa_release",
+            "gqa_decode_noalloc")
 
 _lib = None
 
@@ -53,8 +55,9 @@ def load_library():
     lib.gqa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.gqa_prefill.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
     lib.gqa_decode_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.gqa_prefill_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
-    for fn in ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host"):
+    for fn in ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host", "gqa_decode_noalloc"):
         getattr(lib, fn).restype = i
     lib.gqa_status_string.argtypes = [i]
     lib.gqa_status_string.restype = ctypes.c_char_p
@@ -112,6 +115,24 @@ def gqa_decode(q, k_cache, v_cache, seqlens, out=None, scale=None, stream=None):
                             _dev_ptr(out, "out", torch.bfloat16), B, Hq, Hkv, D, Lmax, float(scale),
                             _stream_ptr(stream, q.device))
     _check(st, "gqa_decode")
+    return out
+
+
+def gqa_decode_noalloc(q, k_cache, v_cache, seqlens, out, scale=None, stream=None):
+    """gqa_decode with its workspace in the library's fixed device array: the
+    call allocates nothing (out must be given).  Overlapping calls race."""
+    import torch
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    if scale is None:
+        scale = D ** -0.5
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.gqa_decode_noalloc(_dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k_cache, "k_cache", torch.bfloat16),
+                                    _dev_ptr(v_cache, "v_cache", torch.bfloat16),
+                                    _dev_ptr(seqlens, "seqlens", torch.int32), _dev_ptr(out, "out", torch.bfloat16),
+                                    B, Hq, Hkv, D, Lmax, float(scale), _stream_ptr(stream, q.device))
+    _check(st, "gqa_decode_noalloc")
     return out
 
 

@@ -292,6 +292,7 @@ const char* gqa_status_string(int status) {
       s = "GQA_ERR_NO_DEVICE: " + (g_cuda_msg.empty() ? std::string("no sm_103 device") : g_cuda_msg);
       return s.c_str();
     }
+    case GQA_ERR_TOO_LARGE: return "GQA_ERR_TOO_LARGE: the sizes need more workspace than the fixed scratch of gqa_decode_noalloc";
     default: return "unknown gqa status";
   }
 }

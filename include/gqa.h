@@ -54,7 +54,8 @@ typedef enum gqa_status {
   GQA_ERR_NULL = 3,        /* a required pointer is NULL */
   GQA_ERR_MISALIGNED = 4,  /* a tensor pointer is not 16-byte aligned */
   GQA_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed; see gqa_status_string */
-  GQA_ERR_NO_DEVICE = 6    /* no usable sm_103 device, or the kernels are not loadable */
+  GQA_ERR_NO_DEVICE = 6,   /* no usable sm_103 device, or the kernels are not loadable */
+  GQA_ERR_TOO_LARGE = 7    /* gqa_decode_noalloc: sizes need more than its fixed scratch */
 } gqa_status;
 
 /* Bits of the per-device status word (gqa_get_device_status). */
@@ -130,6 +131,41 @@ GQA_API int gqa_decode_host(const void* q_host, const void* k_cache_host, const 
                     int Lmax, float scale, void* stream);
 GQA_API int gqa_prefill_host(const void* q_host, const void* k_host, const void* v_host, void* out_host,
                      int B, int L, int Hq, int Hkv, int D, int causal, void* stream);
+
+/*
+ * gqa_decode_noalloc -- gqa_decode for callers that must not have the library
+ * allocate device memory: callers that manage all device memory through their
+ * own pool (a serving engine that reserves HBM for its KV cache at start-up,
+ * where a cudaMalloc from a library could fail or fragment the pool), and
+ * callers on a latency-critical path that may not allocate after start-up
+ * because cudaMalloc / cudaFree can synchronise the device.
+ * The paper pages have no counterpart of this call; it is a deployment
+ * variant of gqa_decode.
+ *
+ * Arguments, layouts, results and device-side fallbacks are those of
+ * gqa_decode.  Differences:
+ *   - the split workspace is a fixed device array inside libgqa.so
+ *     (GQA_NOALLOC_SCRATCH_BYTES, held by every GPU that loads the library
+ *     until the process exits); the call makes no cudaMalloc / cudaFree and
+ *     calls no allocating routine;
+ *   - sizes whose workspace exceeds it return GQA_ERR_TOO_LARGE: at most
+ *     GQA_NOALLOC_MAX_PAIRS (b, kv head) pairs (B * Hkv) and
+ *     GQA_NOALLOC_MAX_PART_FLOATS partial floats (one CTA per SM x 2 x G x
+ *     (D + 2)); every workload with G <= 32, D = 128 and B * Hkv <= 8192 fits;
+ *   - the first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture;
+ *   - every call, on every stream, shares the one array: calls that overlap
+ *     on the GPU race and give wrong results -- order them (one stream, or
+ *     events).  Each call clears the parts that must start at zero;
+ *   - the device status bits of this call are kept in the array and are not
+ *     reported by gqa_get_device_status.
+ */
+#define GQA_NOALLOC_MAX_PAIRS 8192
+#define GQA_NOALLOC_MAX_PART_FLOATS 1310720
+#define GQA_NOALLOC_SCRATCH_BYTES (256 + 4 * GQA_NOALLOC_MAX_PAIRS + 4 * GQA_NOALLOC_MAX_PART_FLOATS)
+GQA_API int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* seqlens, void* out, int B, int Hq, int Hkv, int D,
+                               int Lmax, float scale, void* stream);
 
 /* Human-readable text of a status (for GQA_ERR_CUDA it names the CUDA error
  * of the last failure on this host thread).  Never NULL. */
