@@ -10,9 +10,11 @@ per KV head) -- decode is bound by reading the KV cache.  The causal prefill
 (B=4, L=2048, Hq=32, Hkv=8, D=128) is timed in the same run and reported in
 TFLOP/s under "prefill"; the other decode workloads under "decode_workloads".
 
-L2 (126 MB) is flushed by writing a 256 MiB buffer before every timed launch;
-each launch is bracketed by its own CUDA events on the launching stream, and
-ms_per_step is the mean of those event intervals.
+L2 (126 MB) is flushed before every timed launch: a 256 MiB buffer is written,
+then a second 256 MiB buffer is read, so that the flush's own dirty lines are
+written back before the launch instead of during it.  Each launch is bracketed
+by its own CUDA events on the launching stream, and ms_per_step is the mean of
+those event intervals.
 
 Under torchrun (N > 1) every rank runs its own batch of the same shape
 (independent sequences: no data-path collective; weak scaling); the value is
@@ -124,18 +126,34 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ timing
+class L2Flush:
+    """Evicts L2 (126 MB on B300): writes a 256 MiB buffer, then reads another
+    256 MiB buffer so the written lines are cleaned out before the next launch."""
+
+    def __init__(self, dev, nbytes=256 * 2**20):
+        import torch
+        self.w = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(nbytes // 8, dtype=torch.int64, device=dev)
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.sink)
+
+
 def timed_launches(fn, steps, warmup, flush, stream):
     """Runs fn() warmup times, then `steps` times with an L2 flush before each
     launch; returns the per-launch event durations in ms."""
     import torch
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         fn()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
-        flush.zero_()
+        flush()
         starts[i].record(stream)
         fn()
         ends[i].record(stream)
@@ -287,6 +305,25 @@ def run_reference(args, rank, world):
     return 0
 
 
+def run_only(g, W, args, dev, flush, peaks):
+    """One workload, for profiling and sweeps: prints the per-launch mean time and rate."""
+    if args.only == "prefill":
+        r = bench_prefill(g, W, dev, args.steps, args.warmup, flush)
+        if r is None:
+            print(json.dumps({"only": "prefill", "status": "not built"}))
+            return 0
+        ms = statistics.mean(r["ms"])
+        tf = r["flops"] / (ms / 1e3) / 1e12
+        print(json.dumps({"only": "prefill", "us": ms * 1e3, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]}))
+        return 0
+    r = bench_decode(g, W, args.only, dev, args.steps, args.warmup, flush)
+    ms = statistics.mean(r["ms"])
+    gbs = r["bytes"] / (ms / 1e3) / 1e9
+    print(json.dumps({"only": args.only, "us": ms * 1e3, "us_min": min(r["ms"]) * 1e3, "GB/s": gbs,
+                      "frac": gbs / peaks["hbm_gbs"]}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -296,6 +333,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="headline only (for profiling runs)")
+    ap.add_argument("--only", default=None, help="time one workload (a decode name or 'prefill') and print its line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -314,7 +352,9 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks = load_peaks()
-    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
+    if args.only:
+        return run_only(g, W, args, dev, flush, peaks)
 
     barrier(world)
     with ClockSampler(local) as clocks:
@@ -369,7 +409,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "llama3_8b decode: B=16, Hq=32, Hkv=8, D=128, L=4096 (bf16 KV cache "
                                    "[16, 8, 4096, 128] + q [16, 32, 128], N(0,1) seed 2)",
-                       "l2": "flushed (256 MiB write) before every timed launch",
+                       "l2": "flushed before every timed launch (256 MiB write, then 256 MiB read of another buffer)",
                        "parallelism": f"replica per GPU x{world}" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],

@@ -52,6 +52,7 @@ constexpr int kKW = kBN / 16;      // key-slice warps
 constexpr int kMaxBatch = 1024;    // batches whose tile prefix fits in shared memory
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448; // opt-in dynamic shared memory per CTA on sm_100-class parts
+constexpr int kMaxCtas = 160;      // persistent CTAs at most (one per SM; B300 has 148)
 
 struct Params {
   const __nv_bfloat16* q;
@@ -79,7 +80,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int Gpad) {
   s.k_bytes = (D / 64) * kBN * 128;
   s.stage_bytes = 2 * s.k_bytes;
   s.epi_off = stages * s.stage_bytes;
-  s.red_off = s.epi_off + kKW * Gpad * (D + 4) * 4;
+  // epi holds the key-slice accumulators, later the merge statistics (2 x pieces x G)
+  s.red_off = s.epi_off + (kKW * (D + 4) > 2 * kMaxCtas ? kKW * (D + 4) : 2 * kMaxCtas) * Gpad * 4;
   s.pre_off = s.red_off + 2 * kKW * Gpad * 4;
   s.bar_off = round_up(s.pre_off + (kMaxBatch + 1) * 4, 8);
   s.flag_off = s.bar_off + 2 * stages * 8;
@@ -436,72 +438,135 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
         const int slot = seg_lt0 == 0 ? 1 : 0;
         const size_t slot_idx = (size_t)blockIdx.x * 2 + slot;
         __nv_bfloat16* outp = p.out + ((size_t)it.b * p.Hq + (size_t)it.j * G) * D;
-        for (int e = tid; e < G * (D / 2); e += cthreads) {
-          const int h = e / (D / 2), d = 2 * (e % (D / 2));
+
+        // Per head: the piece's max M, the key slices' weights 2^(m_k - M)
+        // (stored over red_m) and the piece's sum L (stored in red_l[0]).
+        for (int h = tid; h < G; h += cthreads) {
           float M = -INFINITY;
 #pragma unroll
           for (int k = 0; k < kKW; ++k) M = fmaxf(M, red_m[k * Gpad + h]);
           const float Mu = M == -INFINITY ? 0.f : M;
-          float Ls = 0.f, s0 = 0.f, s1 = 0.f;
+          float Ls = 0.f;
 #pragma unroll
           for (int k = 0; k < kKW; ++k) {
             const float f = fast_exp2(red_m[k * Gpad + h] - Mu);
-            const float* ep = epi + (size_t)(k * Gpad + h) * (D + 4) + d;
             Ls += f * red_l[k * Gpad + h];
-            s0 += f * ep[0];
-            s1 += f * ep[1];
+            red_m[k * Gpad + h] = f;
+          }
+          red_l[h] = Ls;
+          red_l[Gpad + h] = M;
+        }
+        named_bar_sync(1, cthreads);
+        for (int e = tid; e < G * (D / 4); e += cthreads) {
+          const int h = e / (D / 4), d = 4 * (e % (D / 4));
+          float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < kKW; ++k) {
+            const float f = red_m[k * Gpad + h];
+            const float4 x = *reinterpret_cast<const float4*>(epi + (size_t)(k * Gpad + h) * (D + 4) + d);
+            acc4.x += f * x.x;
+            acc4.y += f * x.y;
+            acc4.z += f * x.z;
+            acc4.w += f * x.w;
           }
           if (complete) {
-            const float inv = 1.f / Ls;
-            *reinterpret_cast<__nv_bfloat162*>(outp + (size_t)h * D + d) = __floats2bfloat162_rn(s0 * inv, s1 * inv);
+            const float inv = 1.f / red_l[h];
+            uint2 pk;
+            pk.x = pack_bf16x2(acc4.x * inv, acc4.y * inv);
+            pk.y = pack_bf16x2(acc4.z * inv, acc4.w * inv);
+            *reinterpret_cast<uint2*>(outp + (size_t)h * D + d) = pk;
           } else {
-            float* pa = p.part_acc + (slot_idx * G + h) * D + d;
-            pa[0] = s0;
-            pa[1] = s1;
+            *reinterpret_cast<float4*>(p.part_acc + (slot_idx * G + h) * D + d) = acc4;
             if (d == 0) {
-              p.part_ml[(slot_idx * 2 + 0) * G + h] = M;
-              p.part_ml[(slot_idx * 2 + 1) * G + h] = Ls;
+              p.part_ml[(slot_idx * 2 + 0) * G + h] = red_l[Gpad + h];
+              p.part_ml[(slot_idx * 2 + 1) * G + h] = red_l[h];
             }
           }
         }
 
         if (!complete) {
-          __threadfence();
+          // Publish this piece: the barrier orders every thread's partial
+          // stores before thread 0's device-scope fence and arrival.
           named_bar_sync(1, cthreads);
           if (tid == 0) {
             const long long o_p = (long long)Hkv * pre[it.b] + (long long)it.j * it.nb;
             const int c_lo = cta_of(o_p, T, P);
             const int c_hi = cta_of(o_p + it.nb - 1, T, P);
+            __threadfence();
             const int old = atomicAdd(&p.counters[pair], 1);
             const bool last = old == c_hi - c_lo;
-            if (last) p.counters[pair] = 0;  // ready for the next call
+            if (last) {
+              p.counters[pair] = 0;  // ready for the next call
+              __threadfence();
+            }
             *last_flag = last ? (c_lo + 1) : 0;  // encodes c_lo
             *chi_flag = c_hi;
           }
           named_bar_sync(1, cthreads);
           const int lf = *last_flag;
           if (lf) {
-            __threadfence();
-            const int c_lo = lf - 1, c_hi = *chi_flag;
-            for (int e = tid; e < G * (D / 2); e += cthreads) {
-              const int h = e / (D / 2), d = 2 * (e % (D / 2));
+            // This CTA finished the pair's last piece: merge all pieces.
+            // Piece s of the pair sits in CTA c_lo + s, slot 1 for s = 0
+            // (the piece that starts the pair) and slot 0 after it.
+            const int c_lo = lf - 1, nseg = *chi_flag - c_lo + 1;
+            float* wm = epi;              // [nseg][G] piece max, then merge weight
+            float* wl = epi + nseg * G;   // [nseg][G] piece sum
+            for (int e = tid; e < nseg * G; e += cthreads) {
+              const int s2 = e / G, h = e % G;
+              const size_t si = (size_t)(c_lo + s2) * 2 + (s2 == 0 ? 1 : 0);
+              wm[e] = __ldcg(p.part_ml + (si * 2 + 0) * G + h);
+              wl[e] = __ldcg(p.part_ml + (si * 2 + 1) * G + h);
+            }
+            named_bar_sync(1, cthreads);
+            for (int h = tid; h < G; h += cthreads) {
               float M = -INFINITY;
-              for (int c = c_lo; c <= c_hi; ++c) {
-                const size_t si = (size_t)c * 2 + (c == c_lo ? 1 : 0);
-                M = fmaxf(M, __ldcg(p.part_ml + (si * 2 + 0) * G + h));
-              }
+              for (int s2 = 0; s2 < nseg; ++s2) M = fmaxf(M, wm[s2 * G + h]);
               const float Mu = M == -INFINITY ? 0.f : M;
-              float Ls = 0.f, s0 = 0.f, s1 = 0.f;
-              for (int c = c_lo; c <= c_hi; ++c) {
-                const size_t si = (size_t)c * 2 + (c == c_lo ? 1 : 0);
-                const float f = fast_exp2(__ldcg(p.part_ml + (si * 2 + 0) * G + h) - Mu);
-                Ls += f * __ldcg(p.part_ml + (si * 2 + 1) * G + h);
-                const float2 a2 = __ldcg(reinterpret_cast<const float2*>(p.part_acc + (si * G + h) * D + d));
-                s0 += f * a2.x;
-                s1 += f * a2.y;
+              float Ls = 0.f;
+              for (int s2 = 0; s2 < nseg; ++s2) {
+                const float f = fast_exp2(wm[s2 * G + h] - Mu);
+                Ls += f * wl[s2 * G + h];
+                wm[s2 * G + h] = f;
               }
               const float inv = 1.f / Ls;
-              *reinterpret_cast<__nv_bfloat162*>(outp + (size_t)h * D + d) = __floats2bfloat162_rn(s0 * inv, s1 * inv);
+              for (int s2 = 0; s2 < nseg; ++s2) wm[s2 * G + h] *= inv;
+            }
+            named_bar_sync(1, cthreads);
+            // Every thread owns up to 4 float4 chunks of the [G][D] output and
+            // loads its chunks of all pieces without waiting in between.
+            constexpr int kChunksMax = 4;
+            const int nchunk = G * (D / 4);
+            float4 a4[kChunksMax];
+#pragma unroll
+            for (int u = 0; u < kChunksMax; ++u) a4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+            for (int s2 = 0; s2 < nseg; ++s2) {
+              const size_t si = (size_t)(c_lo + s2) * 2 + (s2 == 0 ? 1 : 0);
+              const float* base = p.part_acc + si * G * D;
+#pragma unroll
+              for (int u = 0; u < kChunksMax; ++u) {
+                const int e = tid + u * cthreads;
+                if (e < nchunk) {
+                  const int h = e / (D / 4), d = 4 * (e % (D / 4));
+                  const float f = wm[s2 * G + h];
+                  const float4 x = __ldcg(reinterpret_cast<const float4*>(base + (size_t)h * D + d));
+                  a4[u].x += f * x.x;
+                  a4[u].y += f * x.y;
+                  a4[u].z += f * x.z;
+                  a4[u].w += f * x.w;
+                }
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < kChunksMax; ++u) {
+              const int e = tid + u * cthreads;
+              if (e < nchunk) {
+                const int h = e / (D / 4), d = 4 * (e % (D / 4));
+                uint2 pk;
+                pk.x = pack_bf16x2(a4[u].x, a4[u].y);
+                pk.y = pack_bf16x2(a4[u].z, a4[u].w);
+                *reinterpret_cast<uint2*>(outp + (size_t)h * D + d) = pk;
+              }
             }
           }
         }
@@ -548,7 +613,7 @@ cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t s
 
 }  // namespace
 
-bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan) {
+bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan, size_t max_part_floats) {
   if (B < 1 || B > kMaxBatch || Hkv < 1 || Hq % Hkv != 0 || Lmax < 1) return false;
   if (D != 64 && D != 128) return false;
   const int G = Hq / Hkv;
@@ -568,13 +633,16 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
   plan->tile_keys = kBN;
   plan->threads = 32 * (kKW * HS + 1);
   const long long tiles_max = (long long)B * Hkv * ((Lmax + kBN - 1) / kBN);
-  plan->num_ctas = (int)std::min<long long>(tiles_max, std::max(1, sm_count));
+  plan->num_ctas = (int)std::min<long long>(tiles_max, std::min(kMaxCtas, std::max(1, sm_count)));
   SmemLayout l0 = D == 64 ? smem_layout<64>(0, Gpad) : smem_layout<128>(0, Gpad);
   const int stages = std::min(kMaxStages, (kSmemLimit - l0.total - 2 * kMaxStages * 8) / l0.stage_bytes);
   if (stages < 2) return false;
   plan->stages = stages;
   plan->smem_bytes = (size_t)(D == 64 ? smem_layout<64>(stages, Gpad) : smem_layout<128>(stages, Gpad)).total;
   plan->ws_part_floats = (size_t)plan->num_ctas * 2 * G * (D + 2);
+  if (max_part_floats > 0 && plan->ws_part_floats > max_part_floats) return false;
+  plan->chunk_tiles = 0;  // static split: one contiguous share per CTA
+  plan->chunks_max = plan->num_ctas;
   plan->ws_counters = (size_t)B * Hkv;
   return true;
 }

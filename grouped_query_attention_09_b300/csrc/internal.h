@@ -17,6 +17,8 @@ CUresult encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t dim0, 
 struct DecodePlan {
   int D, G, Gpad, NT, HS;  // head dim, group size, padded group, n-tiles/warp, head slices
   int tile_keys;           // keys per pipeline tile
+  int chunk_tiles;         // tiles per scheduling chunk (unit of work a CTA claims)
+  int chunks_max;          // chunks of a full cache (sizes the partial-result slots)
   int num_ctas;            // persistent CTAs
   int threads;             // threads per CTA
   int stages;              // pipeline depth
@@ -25,9 +27,12 @@ struct DecodePlan {
   size_t ws_counters;      // per-(b, kv head) arrival counters
 };
 
-// Chooses tile size, persistent grid and pipeline depth; returns false if the
-// shape is not supported by the decode kernels.
-bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan);
+// Chooses tile and chunk size, persistent grid and pipeline depth; returns
+// false if the shape is not supported by the decode kernels.  A non-zero
+// max_part_floats bounds the partial-result workspace: the chunks grow
+// coarser until it fits.
+bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan,
+                 size_t max_part_floats = 0);
 
 struct DecodeArgs {
   const void* q;

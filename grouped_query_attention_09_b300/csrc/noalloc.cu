@@ -20,12 +20,13 @@
 
 namespace {
 
-// Scratch layout: [0, 256) status word; [256, 256 + 4*kMaxPairs) arrival
-// counters; then the partial results (fp32).  Total 5 MiB + 33 KiB.
+// Scratch layout: [0, 256) status word; then the arrival counters (one per
+// (b, kv head) pair, two spare); then the partial results (fp32).  Total
+// about 5 MiB + 33 KiB.
 constexpr size_t kMaxPairs = GQA_NOALLOC_MAX_PAIRS;
 constexpr size_t kMaxPartFloats = GQA_NOALLOC_MAX_PART_FLOATS;
 constexpr size_t kCountersOff = 256;
-constexpr size_t kPartOff = (kCountersOff + 4 * kMaxPairs + 255) / 256 * 256;
+constexpr size_t kPartOff = (kCountersOff + 4 * (kMaxPairs + 2) + 255) / 256 * 256;
 constexpr size_t kScratchBytes = kPartOff + 4 * kMaxPartFloats;
 
 // Every GPU that loads the library holds this array until the process exits.
@@ -84,8 +85,9 @@ extern "C" int gqa_decode_noalloc(const void* q, const void* k_cache, const void
   int st = scratch_for_current_device(&base, &sms);
   if (st != GQA_OK) return st;
   gqa::DecodePlan plan;
+  if ((size_t)B * Hkv > kMaxPairs) return GQA_ERR_TOO_LARGE;
   if (!gqa::decode_plan(B, Hq, Hkv, D, Lmax, sms, &plan)) return GQA_ERR_UNSUPPORTED;
-  if (plan.ws_counters > kMaxPairs || plan.ws_part_floats > kMaxPartFloats) return GQA_ERR_TOO_LARGE;
+  if (plan.ws_counters > kMaxPairs + 2 || plan.ws_part_floats > kMaxPartFloats) return GQA_ERR_TOO_LARGE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* b = static_cast<unsigned char*>(base);
   // The array keeps the previous call's contents: the status word and the

@@ -162,7 +162,7 @@ GQA_API int gqa_prefill_host(const void* q_host, const void* k_host, const void*
  */
 #define GQA_NOALLOC_MAX_PAIRS 8192
 #define GQA_NOALLOC_MAX_PART_FLOATS 1310720
-#define GQA_NOALLOC_SCRATCH_BYTES (256 + 4 * GQA_NOALLOC_MAX_PAIRS + 4 * GQA_NOALLOC_MAX_PART_FLOATS)
+#define GQA_NOALLOC_SCRATCH_BYTES (256 + 4 * (GQA_NOALLOC_MAX_PAIRS + 2) + 4 * GQA_NOALLOC_MAX_PART_FLOATS)
 GQA_API int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* seqlens, void* out, int B, int Hq, int Hkv, int D,
                                int Lmax, float scale, void* stream);
