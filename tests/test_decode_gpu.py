@@ -1,34 +1,16 @@
 """Decode parity: the CUDA path (through the C ABI) against the fp64 oracle.
 
-Bar (written here, applied element-wise): |gpu - oracle| <= 1e-2 + 1e-2 |oracle|
-on the same seeded bf16 inputs.  The kernel accumulates in fp32, rounds the
-softmax weights to bf16 before P V and rounds the output to bf16; at |out|
-<= ~4 the bf16 output rounding alone is up to 2^-9 |out|, well inside the bar.
+Bar (tests/parity.py, applied element-wise): |gpu - oracle| <= 1e-2 + 1e-2 |oracle|
+on the same seeded bf16 inputs.
 """
 import numpy as np
 import pytest
 import torch
 
 from grouped_query_attention_09_b300 import workloads as W
+from parity import assert_parity
 
 pytestmark = pytest.mark.gpu
-
-ATOL = 1e-2
-RTOL = 1e-2
-
-
-def assert_parity(gpu, ref, what=""):
-    gpu = np.asarray(gpu, dtype=np.float64)
-    ref = np.asarray(ref, dtype=np.float64)
-    assert gpu.shape == ref.shape
-    assert np.isfinite(gpu).all(), f"{what}: non-finite output"
-    err = np.abs(gpu - ref)
-    bound = ATOL + RTOL * np.abs(ref)
-    bad = err > bound
-    if bad.any():
-        idx = np.unravel_index(np.argmax(err - bound), err.shape)
-        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; worst at {idx}: "
-                             f"gpu={gpu[idx]!r} oracle={ref[idx]!r}")
 
 
 def run_decode(g, q, k, v, sl, scale, dev, stream=None):

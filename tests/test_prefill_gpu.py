@@ -1,0 +1,105 @@
+"""Prefill parity: the tcgen05 CUDA path (through the C ABI) against the fp64
+oracle, at the bar of tests/parity.py.
+
+Small shapes are compared element by element; they span several 128-row
+query tiles and 128-key blocks, ragged tails, both causal settings, even G
+(two query heads share each K/V block) and odd G (one head per unit), the MHA
+and MQA endpoints, and grids where every CTA walks several units.  The
+full-size causal workload (B=4, L=2048, Hq=32, Hkv=8, D=128) is checked on
+sampled rows, in the launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+from grouped_query_attention_09_b300 import workloads as W
+from parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(g, q, k, v, causal, dev):
+    out = g.gqa_prefill(q.to(dev), k.to(dev), v.to(dev), causal=causal)
+    flags = g.gqa_get_device_status()
+    return out.cpu(), flags
+
+
+def oracle_prefill(oracle_mod, q, k, v, causal, rows=None):
+    return oracle_mod.prefill(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), causal=causal, rows=rows)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L,causal", [
+    (1, 2, 1, 128, True),      # one unit: two heads, one tile, one diagonal block
+    (1, 4, 2, 300, True),      # ragged last tile, three query tiles
+    (2, 8, 2, 129, False),     # full attention, ragged last key block
+    (1, 3, 1, 200, True),      # odd G: one head per unit
+    (1, 4, 4, 256, True),      # MHA endpoint
+    (1, 8, 1, 1, True),        # a single token
+    (1, 2, 1, 100, False),     # shorter than one tile
+    (1, 32, 1, 640, True),     # MQA endpoint, G = 32
+    (2, 6, 3, 384, False),     # G = 2, full attention
+    (4, 16, 4, 1152, True),    # 288 units: every CTA walks two of them
+])
+def test_shapes_parity(gqa_lib, oracle_mod, cuda_device, B, Hq, Hkv, L, causal):
+    w = W.PrefillWorkload("case", B, L, Hq, Hkv, 128, causal, 500 + B * Hq + L)
+    q, k, v = W.make_prefill_inputs(w)
+    out, flags = run_prefill(gqa_lib, q, k, v, causal, cuda_device)
+    assert flags == 0
+    ref = oracle_prefill(oracle_mod, q, k, v, causal)
+    assert_parity(out.double().numpy(), ref, f"{B},{Hq},{Hkv},{L},{causal}")
+
+
+def test_peaky_softmax_rebases_running_max(gqa_lib, oracle_mod, cuda_device):
+    """q x 8: logits with a spread of tens, so the running max of a row grows
+    by more than the re-base margin from block to block and the rescale of the
+    partial output is exercised."""
+    w = W.PrefillWorkload("peaky", 2, 768, 8, 2, 128, True, 71)
+    q, k, v = W.make_prefill_inputs(w, q_mult=8.0)
+    for causal in (True, False):
+        out, flags = run_prefill(gqa_lib, q, k, v, causal, cuda_device)
+        assert flags == 0
+        assert_parity(out.double().numpy(), oracle_prefill(oracle_mod, q, k, v, causal), f"peaky causal={causal}")
+
+
+def _sample_rows(w, rng, n_random=48):
+    heads = sorted({0, 1, 2, 3, w.G if hasattr(w, "G") else 4, w.Hq // 2 + 1, w.Hq - 1})
+    fixed = [0, 1, 2, 63, 127, 128, 129, 255, 1023, 1024, w.L - 129, w.L - 128, w.L - 2, w.L - 1]
+    rows = []
+    for b in range(w.B):
+        for h in heads:
+            idx = set(i for i in fixed if 0 <= i < w.L) | set(rng.integers(0, w.L, n_random).tolist())
+            rows += [(b, h, i) for i in sorted(idx)]
+    return np.array(rows, dtype=np.int32)
+
+
+def test_full_size_causal_workload_sampled_rows(gqa_lib, oracle_mod, cuda_device):
+    """The benchmark's prefill workload at full size; rows sampled across every
+    batch, first/middle/last heads of several groups, tile edges and the end."""
+    w = W.WORKLOADS["prefill"]
+    q, k, v = W.make_prefill_inputs(w)
+    out, flags = run_prefill(gqa_lib, q, k, v, w.causal, cuda_device)
+    assert flags == 0
+    rows = _sample_rows(w, np.random.default_rng(5))
+    ref = oracle_prefill(oracle_mod, q, k, v, w.causal, rows=rows)
+    got = out[rows[:, 0], rows[:, 1], rows[:, 2]].double().numpy()
+    assert_parity(got, ref, "prefill full size")
+    assert torch.isfinite(out.float()).all()
+
+
+def test_repeatable_side_stream_and_host_entry(gqa_lib, cuda_device):
+    """Identical calls give identical bits, on another stream too, and
+    gqa_prefill_host on host buffers matches gqa_prefill on device buffers."""
+    w = W.PrefillWorkload("rep", 2, 640, 8, 2, 128, True, 81)
+    q, k, v = W.make_prefill_inputs(w)
+    qd, kd, vd = q.to(cuda_device), k.to(cuda_device), v.to(cuda_device)
+    a = gqa_lib.gqa_prefill(qd, kd, vd).clone()
+    s = torch.cuda.Stream(cuda_device)
+    s.wait_stream(torch.cuda.current_stream(cuda_device))
+    with torch.cuda.stream(s):
+        b = gqa_lib.gqa_prefill(qd, kd, vd, stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    host = gqa_lib.gqa_prefill_host(q.pin_memory(), k.pin_memory(), v.pin_memory())
+    assert torch.equal(a.cpu(), host)
+    assert gqa_lib.gqa_get_device_status() == 0
