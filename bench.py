@@ -49,6 +49,9 @@ NCU_TRAFFIC = {
     "decode.cu": {"sha256": "bfd045a7080e8b19c4956137daf91f93079f339ac5440bc3458bd15ea3e13d30",
                   "bytes_per_launch": 271602176.0,
                   "capture": "ncu --set full, llama3_8b decode (dram__bytes_read.sum + dram__bytes_write.sum)"},
+    "prefill.cu": {"sha256": "da92ceaa6163c89fde6c9c5481f4f5266dc3d41080f391b025e3afe4f0ec4c42",
+                   "bytes_per_launch": 115568640.0,
+                   "capture": "ncu --set full, causal prefill B=4 L=2048 (dram__bytes_read.sum + dram__bytes_write.sum)"},
 }
 
 
