@@ -51,7 +51,7 @@ namespace {
 constexpr int kD = 128;          // head dim
 constexpr int kBM = 128;         // query rows per tile
 constexpr int kBN = 128;         // keys per block
-constexpr int kStages = 3;       // K/V ring depth (a slot holds one K or one V block)
+constexpr int kStages = 5;       // K/V ring depth (a slot holds one K or one V block)
 constexpr int kTileBytes = kBM * kD * 2;  // 32 KiB: one Q tile, P tile, K or V block
 constexpr int kHalfBytes = kTileBytes / 2;  // one 64-column half (128-byte rows)
 constexpr int kThreads = 320;
@@ -62,8 +62,7 @@ constexpr float kRebaseLog2 = 8.0f;  // re-base the running max when it grows by
 
 // Shared memory (offsets from a 1024-byte aligned base).
 constexpr int kOffQ = 0;                              // 2 query tiles
-constexpr int kOffP = kOffQ + 2 * kTileBytes;         // 2 P tiles (bf16)
-constexpr int kOffRing = kOffP + 2 * kTileBytes;      // kStages K/V blocks
+constexpr int kOffRing = kOffQ + 2 * kTileBytes;      // kStages K/V blocks
 constexpr int kOffBars = kOffRing + kStages * kTileBytes;
 constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;     // TMEM base, abort flag
@@ -173,8 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
       uint32_t kv_it = 0;
-      int slot_used[kStages] = {0, 0, 0};
-      uint32_t slot_par[kStages] = {0, 0, 0};
+      int slot_used[kStages] = {};
+      uint32_t slot_par[kStages] = {};
       int q_used = 0;
       bool ok = true;
       int i = 0;
@@ -220,7 +219,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kBM, kD, true);
       const uint32_t q_addr = smem_u32(smem + kOffQ);
-      const uint32_t p_addr = smem_u32(smem + kOffP);
       const uint32_t ring_addr = smem_u32(smem + kOffRing);
       auto issue_s = [&](int t, int slot) {
         const uint32_t a0 = q_addr + t * kTileBytes, b0 = ring_addr + slot * kTileBytes;
@@ -231,12 +229,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                      idesc_s, k > 0);
         }
       };
+      // P_t sits in TMEM columns [128t, 128t + 64) (over the S_t it came
+      // from), 16 keys = 8 columns per instruction.
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t a0 = p_addr + t * kTileBytes, b0 = ring_addr + slot * kTileBytes;
+        const uint32_t b0 = ring_addr + slot * kTileBytes;
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
-          const uint32_t aoff = (k >> 2) * kHalfBytes + (k & 3) * 32;
-          tc::mma_ss(tmem + 256 + t * 128, tc::sdesc_sw128(a0 + aoff, 16, 1024),
+          tc::mma_ts(tmem + 256 + t * 128, tmem + t * 128 + k * 8,
                      tc::sdesc_sw128(b0 + k * 16 * 128, kHalfBytes, 1024), idesc_o, (acc || k > 0) ? 1u : 0u);
         }
       };
@@ -314,8 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_tm = tmem + lane_addr + t * 128;
     const uint32_t o_tm = tmem + lane_addr + 256 + t * 128;
-    uint8_t* prow = smem + kOffP + t * kTileBytes + r * 128;
-    const int sw = r & 7;
     uint32_t sc = 0, oc = 0;
     bool ok = (t == 0) || p.two;
     int i = 0;
@@ -346,11 +343,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e)
               if (key0 + c * 32 + e > lim) s[c][e] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // Row max: 16 independent chains, then a tree.
+        float mxv[16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int e = 0; e < 16; ++e) mxv[e] = fmaxf(__uint_as_float(s[0][e]), __uint_as_float(s[0][e + 16]));
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+        for (int c = 1; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            mxv[e] = fmaxf(mxv[e], fmaxf(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 16])));
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int e = 0; e < w; ++e) mxv[e] = fmaxf(mxv[e], mxv[e + w]);
+        const float mx = mxv[0];
         const float mxs = mx * p.scale_log2;
         const bool rebase = mxs > m_use + kRebaseLog2;
         const bool any_rebase = __any_sync(0xffffffffu, rebase);
@@ -358,24 +364,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = rebase ? fast_exp2(m_use - m_new) : 1.f;
         m_use = m_new;
         const float ref = (m_use == -INFINITY) ? 0.f : m_use;
-        float lsum = 0.f;
+        // P = exp2(S * scale * log2e - ref) as bf16 pairs, written over the
+        // first 64 TMEM columns of S_t (row r = lane r).
+        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          uint32_t pw[16];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {  // 8 keys = one 16-byte chunk
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float p0 = fast_exp2(fmaf(__uint_as_float(s[c][g * 8 + 2 * e]), p.scale_log2, -ref));
-              const float p1 = fast_exp2(fmaf(__uint_as_float(s[c][g * 8 + 2 * e + 1]), p.scale_log2, -ref));
-              lsum += p0 + p1;
-              w[e] = pack_bf16x2(p0, p1);
-            }
-            const int chunk = c * 4 + g;  // 0..15 along the keys
-            uint8_t* dst = prow + (chunk >> 3) * kHalfBytes + (((chunk & 7) ^ sw) << 4);
-            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(s[c][2 * e]), p.scale_log2, -ref));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(s[c][2 * e + 1]), p.scale_log2, -ref));
+            ls[e & 7] += p0 + p1;
+            pw[e] = pack_bf16x2(p0, p1);
           }
+          tc::st_32x32b_x16(s_tm + c * 16, pw);
         }
+        const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         l = l * alpha + lsum;
         // O holds the blocks before this one (the commit that signalled S
         // also covered the previous P V); bring it to the new reference.
@@ -389,9 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
             tc::st_32x32b_x32(o_tm + c * 32, o);
           }
-          tc::wait_st();
         }
-        fence_proxy_async_smem();
+        tc::wait_st();
         tc::fence_before_sync();
         mbar_arrive(&p_full[t]);
       }
