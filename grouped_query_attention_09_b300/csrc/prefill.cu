@@ -172,8 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
       uint32_t kv_it = 0;
-      int slot_used[kStages] = {};
-      uint32_t slot_par[kStages] = {};
+      uint32_t slot_used = 0, slot_par = 0;  // bit s: slot s was loaded / its last parity
       int q_used = 0;
       bool ok = true;
       int i = 0;
@@ -201,111 +200,126 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&kv_full[s], kTileBytes);
             tma_load_3d(dst, m, 0, jb * kBN, kvrow, &kv_full[s], pol_kv);
             tma_load_3d(dst + kHalfBytes, m, 64, jb * kBN, kvrow, &kv_full[s], pol_kv);
-            slot_used[s] = 1;
-            slot_par[s] = par;
+            slot_used |= 1u << s;
+            slot_par = (slot_par & ~(1u << s)) | (par << s);
             ++kv_it;
           }
         }
       }
       // Drain: every copy this thread started has landed before the CTA exits.
       for (int s = 0; s < kStages; ++s)
-        if (slot_used[s]) mbar_wait_drain(&kv_full[s], slot_par[s], p.err);
+        if (slot_used >> s & 1u) mbar_wait_drain(&kv_full[s], slot_par >> s & 1u, p.err);
       if (q_used)
         for (int t = 0; t < 1 + p.two; ++t) mbar_wait_drain(&q_full[t], (q_used - 1) & 1, p.err);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false);
-      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kBM, kD, true);
-      const uint32_t q_addr = smem_u32(smem + kOffQ);
-      const uint32_t ring_addr = smem_u32(smem + kOffRing);
-      auto issue_s = [&](int t, int slot) {
-        const uint32_t a0 = q_addr + t * kTileBytes, b0 = ring_addr + slot * kTileBytes;
+    // The whole warp walks the schedule and waits on the barriers, so that
+    // every descriptor is a warp-uniform value; one elected lane issues the
+    // MMAs and the commits that track them.
+    constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false);
+    constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kBM, kD, true);
+    const bool leader = elect_one_sync();
+    // Descriptors of the tile bases; the address field (bits 0-13, in 16-byte
+    // units) is advanced by adding the byte offset >> 4 (no carry: smem < 256 KiB).
+    const uint64_t dq = tc::sdesc_sw128(smem_u32(smem + kOffQ), 16, 1024);
+    const uint64_t dk = tc::sdesc_sw128(smem_u32(smem + kOffRing), 16, 1024);
+    const uint64_t dv = tc::sdesc_sw128(smem_u32(smem + kOffRing), kHalfBytes, 1024);
+    auto issue_s = [&](int t, int slot) {
+      const uint64_t a0 = dq + (uint64_t)((t * kTileBytes) >> 4);
+      const uint64_t b0 = dk + (uint64_t)((slot * kTileBytes) >> 4);
+      if (leader) {
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) {
-          const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-          tc::mma_ss(tmem + t * 128, tc::sdesc_sw128(a0 + off, 16, 1024), tc::sdesc_sw128(b0 + off, 16, 1024),
-                     idesc_s, k > 0);
-        }
-      };
-      // P_t sits in TMEM columns [128t, 128t + 64) (over the S_t it came
-      // from), 16 keys = 8 columns per instruction.
-      auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t b0 = ring_addr + slot * kTileBytes;
-#pragma unroll
-        for (int k = 0; k < kBN / 16; ++k) {
-          tc::mma_ts(tmem + 256 + t * 128, tmem + t * 128 + k * 8,
-                     tc::sdesc_sw128(b0 + k * 16 * 128, kHalfBytes, 1024), idesc_o, (acc || k > 0) ? 1u : 0u);
-        }
-      };
-      uint32_t kv_it = 0, pc0 = 0, pc1 = 0;
-      bool ok = true;
-      int i = 0;
-      for (int u = my_unit(p, 0); u >= 0 && ok; u = my_unit(p, ++i)) {
-        const Unit x = unit_at(p, u);
-        const int nt = 1 + p.two;
-        for (int t = 0; t < nt && ok; ++t) ok = mbar_wait_bounded(&q_full[t], i & 1, abort_flag, p.err);
-        if (!ok) break;
-        int ks = kv_it % kStages;
-        ok = mbar_wait_bounded(&kv_full[ks], (kv_it / kStages) & 1, abort_flag, p.err);
-        if (!ok) break;
-        ++kv_it;
-        tc::fence_after_sync();
-        for (int t = 0; t < nt; ++t) {
-          issue_s(t, ks);
-          tc::commit(&s_full[t]);
-          if (x.n == 1) tc::commit(&q_empty[t]);
-        }
-        tc::commit(&kv_empty[ks]);
-        for (int jb = 0; jb < x.n && ok; ++jb) {
-          const int vs = kv_it % kStages;
-          ok = mbar_wait_bounded(&kv_full[vs], (kv_it / kStages) & 1, abort_flag, p.err);
-          if (!ok) break;
-          ++kv_it;
-          ok = mbar_wait_bounded(&p_full[0], pc0 & 1, abort_flag, p.err);
-          if (!ok) break;
-          ++pc0;
-          tc::fence_after_sync();
-          issue_pv(0, vs, jb > 0);
-          int ks2 = -1;
-          if (jb + 1 < x.n) {
-            ks2 = kv_it % kStages;
-            ok = mbar_wait_bounded(&kv_full[ks2], (kv_it / kStages) & 1, abort_flag, p.err);
-            if (!ok) break;
-            ++kv_it;
-            tc::fence_after_sync();
-            issue_s(0, ks2);
-            tc::commit(&s_full[0]);
-            if (jb + 2 == x.n) tc::commit(&q_empty[0]);
-          } else {
-            tc::commit(&o_full[0]);
-          }
-          if (!p.two) {
-            tc::commit(&kv_empty[vs]);
-            if (ks2 >= 0) tc::commit(&kv_empty[ks2]);
-            continue;
-          }
-          ok = mbar_wait_bounded(&p_full[1], pc1 & 1, abort_flag, p.err);
-          if (!ok) break;
-          ++pc1;
-          tc::fence_after_sync();
-          issue_pv(1, vs, jb > 0);
-          tc::commit(&kv_empty[vs]);
-          if (ks2 >= 0) {
-            issue_s(1, ks2);
-            tc::commit(&s_full[1]);
-            if (jb + 2 == x.n) tc::commit(&q_empty[1]);
-            tc::commit(&kv_empty[ks2]);
-          } else {
-            tc::commit(&o_full[1]);
-          }
+          const uint64_t off = (uint64_t)(((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4);
+          tc::mma_ss(tmem + t * 128, a0 + off, b0 + off, idesc_s, k > 0);
         }
       }
-      // Drain: every MMA this thread issued has completed before TMEM is freed.
-      tc::commit(mma_done);
-      mbar_wait_drain(mma_done, 0, p.err);
+    };
+    // P_t sits in TMEM columns [128t, 128t + 64) (over the S_t it came
+    // from), 16 keys = 8 columns per instruction.
+    auto issue_pv = [&](int t, int slot, bool acc) {
+      const uint64_t b0 = dv + (uint64_t)((slot * kTileBytes) >> 4);
+      if (leader) {
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)
+          tc::mma_ts(tmem + 256 + t * 128, tmem + t * 128 + k * 8, b0 + (uint64_t)((k * 16 * 128) >> 4), idesc_o,
+                     (acc || k > 0) ? 1u : 0u);
+      }
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (leader) tc::commit(bar);
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      const bool w = mbar_wait_bounded(bar, parity, abort_flag, p.err);
+      return __all_sync(0xffffffffu, w);
+    };
+    uint32_t kv_it = 0, pc0 = 0, pc1 = 0;
+    bool ok = true;
+    int i = 0;
+    for (int u = my_unit(p, 0); u >= 0 && ok; u = my_unit(p, ++i)) {
+      const Unit x = unit_at(p, u);
+      const int nt = 1 + p.two;
+      for (int t = 0; t < nt && ok; ++t) ok = wait(&q_full[t], i & 1);
+      if (!ok) break;
+      int ks = kv_it % kStages;
+      ok = wait(&kv_full[ks], (kv_it / kStages) & 1);
+      if (!ok) break;
+      ++kv_it;
+      tc::fence_after_sync();
+      for (int t = 0; t < nt; ++t) {
+        issue_s(t, ks);
+        commit(&s_full[t]);
+        if (x.n == 1) commit(&q_empty[t]);
+      }
+      commit(&kv_empty[ks]);
+      for (int jb = 0; jb < x.n && ok; ++jb) {
+        const int vs = kv_it % kStages;
+        ok = wait(&kv_full[vs], (kv_it / kStages) & 1);
+        if (!ok) break;
+        ++kv_it;
+        ok = wait(&p_full[0], pc0 & 1);
+        if (!ok) break;
+        ++pc0;
+        tc::fence_after_sync();
+        issue_pv(0, vs, jb > 0);
+        int ks2 = -1;
+        if (jb + 1 < x.n) {
+          ks2 = kv_it % kStages;
+          ok = wait(&kv_full[ks2], (kv_it / kStages) & 1);
+          if (!ok) break;
+          ++kv_it;
+          tc::fence_after_sync();
+          issue_s(0, ks2);
+          commit(&s_full[0]);
+          if (jb + 2 == x.n) commit(&q_empty[0]);
+        } else {
+          commit(&o_full[0]);
+        }
+        if (!p.two) {
+          commit(&kv_empty[vs]);
+          if (ks2 >= 0) commit(&kv_empty[ks2]);
+          continue;
+        }
+        ok = wait(&p_full[1], pc1 & 1);
+        if (!ok) break;
+        ++pc1;
+        tc::fence_after_sync();
+        issue_pv(1, vs, jb > 0);
+        commit(&kv_empty[vs]);
+        if (ks2 >= 0) {
+          issue_s(1, ks2);
+          commit(&s_full[1]);
+          if (jb + 2 == x.n) commit(&q_empty[1]);
+          commit(&kv_empty[ks2]);
+        } else {
+          commit(&o_full[1]);
+        }
+      }
     }
+    // Drain: every MMA issued has completed before TMEM is freed.
+    commit(mma_done);
+    mbar_wait_drain(mma_done, 0, p.err);
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;           // query tile 0 or 1
@@ -343,17 +357,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e)
               if (key0 + c * 32 + e > lim) s[c][e] = __float_as_uint(-INFINITY);
         }
-        // Row max: 16 independent chains, then a tree.
-        float mxv[16];
+        // Row max: 8 independent chains, then a tree.
+        float mxv[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) mxv[e] = fmaxf(__uint_as_float(s[0][e]), __uint_as_float(s[0][e + 16]));
+        for (int e = 0; e < 8; ++e)
+          mxv[e] = fmaxf(fmaxf(__uint_as_float(s[0][e]), __uint_as_float(s[0][e + 8])),
+                         fmaxf(__uint_as_float(s[0][e + 16]), __uint_as_float(s[0][e + 24])));
 #pragma unroll
         for (int c = 1; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            mxv[e] = fmaxf(mxv[e], fmaxf(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 16])));
+          for (int e = 0; e < 8; ++e)
+            mxv[e] = fmaxf(mxv[e], fmaxf(fmaxf(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 8])),
+                                         fmaxf(__uint_as_float(s[c][e + 16]), __uint_as_float(s[c][e + 24]))));
 #pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
+        for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int e = 0; e < w; ++e) mxv[e] = fmaxf(mxv[e], mxv[e + w]);
         const float mx = mxv[0];
