@@ -274,22 +274,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       commit(&kv_empty[ks]);
       for (int jb = 0; jb < x.n && ok; ++jb) {
+        // V of this block and K of the next one first: both were usually
+        // loaded long ago, and P0 is the wait on the critical path.
         const int vs = kv_it % kStages;
         ok = wait(&kv_full[vs], (kv_it / kStages) & 1);
         if (!ok) break;
         ++kv_it;
-        ok = wait(&p_full[0], pc0 & 1);
-        if (!ok) break;
-        ++pc0;
-        tc::fence_after_sync();
-        issue_pv(0, vs, jb > 0);
         int ks2 = -1;
         if (jb + 1 < x.n) {
           ks2 = kv_it % kStages;
           ok = wait(&kv_full[ks2], (kv_it / kStages) & 1);
           if (!ok) break;
           ++kv_it;
-          tc::fence_after_sync();
+        }
+        ok = wait(&p_full[0], pc0 & 1);
+        if (!ok) break;
+        ++pc0;
+        tc::fence_after_sync();
+        issue_pv(0, vs, jb > 0);
+        if (ks2 >= 0) {
           issue_s(0, ks2);
           commit(&s_full[0]);
           if (jb + 2 == x.n) commit(&q_empty[0]);
@@ -357,22 +360,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e)
               if (key0 + c * 32 + e > lim) s[c][e] = __float_as_uint(-INFINITY);
         }
-        // Row max: 8 independent chains, then a tree.
+        // Row max: 8 independent chains of 3-input max, then a tree.
         float mxv[8];
+#define SV(i) __uint_as_float(s[(i) >> 5][(i) & 31])
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          mxv[e] = fmaxf(fmaxf(__uint_as_float(s[0][e]), __uint_as_float(s[0][e + 8])),
-                         fmaxf(__uint_as_float(s[0][e + 16]), __uint_as_float(s[0][e + 24])));
+        for (int e = 0; e < 8; ++e) {
+          // chain e takes elements e + 8m, m = 0..15
+          float m = fmax3(SV(e), SV(e + 8), SV(e + 16));
 #pragma unroll
-        for (int c = 1; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            mxv[e] = fmaxf(mxv[e], fmaxf(fmaxf(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 8])),
-                                         fmaxf(__uint_as_float(s[c][e + 16]), __uint_as_float(s[c][e + 24]))));
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int e = 0; e < w; ++e) mxv[e] = fmaxf(mxv[e], mxv[e + w]);
+          for (int q = 3; q < 15; q += 2) m = fmax3(m, SV(e + 8 * q), SV(e + 8 * (q + 1)));
+          mxv[e] = fmaxf(m, SV(e + 120));
+        }
+#undef SV
+        mxv[0] = fmax3(mxv[0], mxv[1], mxv[2]);
+        mxv[3] = fmax3(mxv[3], mxv[4], mxv[5]);
+        mxv[6] = fmaxf(mxv[6], mxv[7]);
+        mxv[0] = fmax3(mxv[0], mxv[3], mxv[6]);
         const float mx = mxv[0];
         const float mxs = mx * p.scale_log2;
         const bool rebase = mxs > m_use + kRebaseLog2;
@@ -384,14 +387,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = exp2(S * scale * log2e - ref) as bf16 pairs, written over the
         // first 64 TMEM columns of S_t (row r = lane r).
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const float sl = p.scale_log2, nref = -ref;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pw[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(s[c][2 * e]), p.scale_log2, -ref));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(s[c][2 * e + 1]), p.scale_log2, -ref));
-            ls[e & 7] += p0 + p1;
+            float x0, x1;
+            fma2(x0, x1, __uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1]), sl, sl, nref, nref);
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            ls[2 * (e & 3)] += p0;
+            ls[2 * (e & 3) + 1] += p1;
             pw[e] = pack_bf16x2(p0, p1);
           }
           tc::st_32x32b_x16(s_tm + c * 16, pw);
