@@ -69,7 +69,7 @@ struct Params {
 
 struct SmemLayout {
   int stage_bytes, k_bytes;
-  int epi_off, red_off, pre_off, bar_off, flag_off, total;
+  int epi_off, red_off, q_off, pre_off, bar_off, flag_off, total;
 };
 
 __host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
@@ -82,7 +82,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int Gpad) {
   s.epi_off = stages * s.stage_bytes;
   // epi holds the key-slice accumulators, later the merge statistics (2 x pieces x G)
   s.red_off = s.epi_off + (kKW * (D + 4) > 2 * kMaxCtas ? kKW * (D + 4) : 2 * kMaxCtas) * Gpad * 4;
-  s.pre_off = s.red_off + 2 * kKW * Gpad * 4;
+  s.q_off = s.red_off + 2 * kKW * Gpad * 4;     // [Gpad][D + 8] bf16 (NT = 2 only)
+  s.pre_off = round_up(s.q_off + Gpad * (D + 8) * 2, 16);
   s.bar_off = round_up(s.pre_off + (kMaxBatch + 1) * 4, 8);
   s.flag_off = s.bar_off + 2 * stages * 8;
   s.total = s.flag_off + 4 * (4 + 32) + 1024;  // flags + scan scratch, + slack to align the base
@@ -274,7 +275,13 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
 
     float acc[KT][NT][4];
     float m_run[NT][2], l_run[NT][2];
-    uint32_t qf[KT][NT][2];
+    // NT = 1 keeps the group's q fragments in registers; NT = 2 (G = 16, 32)
+    // reads them from a padded copy in shared memory with ldmatrix, which
+    // keeps the per-thread state of the wider head slice out of local memory.
+    constexpr int kQReg = NT == 1 ? KT : 1;
+    uint32_t qf[kQReg][NT][2];
+    __nv_bfloat16* q_s = reinterpret_cast<__nv_bfloat16*>(smem + L.q_off);
+    constexpr int kQRow = D + 8;  // padded row (elements): rows 16 B apart in the bank map
     int seg_lt0 = 0, len_b = 0;
     bool live = true;
 
@@ -291,20 +298,30 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
         seg_lt0 = it.lt;
         len_b = clamp_len(p.seqlens[it.b], p.Lmax);
         const __nv_bfloat16* qb = p.q + ((size_t)it.b * p.Hq + (size_t)it.j * G) * D;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int hg = (hs * NT + nt) * 8 + (lane >> 2);
+        if constexpr (NT == 1) {
 #pragma unroll
           for (int kk = 0; kk < KT; ++kk) {
+            const int hg = (lane >> 2);
             if (hg < G) {
               const uint32_t* qp = reinterpret_cast<const uint32_t*>(qb + (size_t)hg * D + kk * 16 + 2 * (lane & 3));
-              qf[kk][nt][0] = __ldg(qp);
-              qf[kk][nt][1] = __ldg(qp + 4);
+              qf[kk][0][0] = __ldg(qp);
+              qf[kk][0][1] = __ldg(qp + 4);
             } else {
-              qf[kk][nt][0] = 0u;
-              qf[kk][nt][1] = 0u;
+              qf[kk][0][0] = 0u;
+              qf[kk][0][1] = 0u;
             }
           }
+        } else {
+          // The previous piece's last named barrier has passed: q_s is free.
+          for (int e = tid; e < G * (D / 8); e += cthreads) {
+            const int h = e / (D / 8), c = e % (D / 8);
+            *reinterpret_cast<uint4*>(q_s + h * kQRow + c * 8) =
+                __ldg(reinterpret_cast<const uint4*>(qb + (size_t)h * D + c * 8));
+          }
+          named_bar_sync(1, cthreads);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             m_run[nt][e] = -INFINITY;
@@ -350,8 +367,19 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
           uint32_t a[4];
           const int chunk = (kk & 3) * 2 + k_chunk_add;
           ldmatrix_x4(a, kbase + (kk >> 2) * kBN * 128 + k_row * 128 + ((chunk ^ sw) << 4));
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], a, qf[kk][nt][0], qf[kk][nt][1]);
+          if constexpr (NT == 1) {
+            mma_bf16_16816(sc[0], a, qf[kk][0][0], qf[kk][0][1]);
+          } else {
+            // B fragments of both n-tiles for this k-step: matrices
+            // (nt, d-lo), (nt, d-hi) for nt = 0, 1; lane l addresses head
+            // row l % 8 of matrix l / 8.
+            uint32_t b[4];
+            const int m = lane >> 3;
+            const int hrow = (hs * NT + (m >> 1)) * 8 + (lane & 7);
+            ldmatrix_x4(b, smem_u32(q_s + hrow * kQRow + kk * 16 + (m & 1) * 8));
+            mma_bf16_16816(sc[0], a, b[0], b[1]);
+            mma_bf16_16816(sc[1], a, b[2], b[3]);
+          }
         }
 
         // ---- online softmax (log2 domain); rows = keys, columns = heads
@@ -431,6 +459,21 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
             e0[d + 8] = acc[mt][nt][2];
             e1[d + 8] = acc[mt][nt][3];
           }
+        }
+        // The running state now lives in shared memory; resetting it here
+        // (the next piece starts from it anyway) frees its registers for the
+        // merge below.
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            m_run[nt][e] = -INFINITY;
+            l_run[nt][e] = 0.f;
+          }
+#pragma unroll
+          for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[kk][nt][e] = 0.f;
         }
         named_bar_sync(1, cthreads);
 
