@@ -74,15 +74,18 @@ struct SmemLayout {
 
 __host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
+// NG: groups of consumer warps that take alternate tiles (each group keeps
+// its own running state, merged at the end of a piece like the key slices).
 template <int D>
-__host__ __device__ inline SmemLayout smem_layout(int stages, int Gpad) {
+__host__ __device__ inline SmemLayout smem_layout(int stages, int Gpad, int NG) {
   SmemLayout s;
+  const int slices = kKW * NG;
   s.k_bytes = (D / 64) * kBN * 128;
   s.stage_bytes = 2 * s.k_bytes;
   s.epi_off = stages * s.stage_bytes;
   // epi holds the key-slice accumulators, later the merge statistics (2 x pieces x G)
-  s.red_off = s.epi_off + (kKW * (D + 4) > 2 * kMaxCtas ? kKW * (D + 4) : 2 * kMaxCtas) * Gpad * 4;
-  s.q_off = s.red_off + 2 * kKW * Gpad * 4;     // [Gpad][D + 8] bf16 (NT = 2 only)
+  s.red_off = s.epi_off + (slices * (D + 4) > 2 * kMaxCtas ? slices * (D + 4) : 2 * kMaxCtas) * Gpad * 4;
+  s.q_off = s.red_off + 2 * slices * Gpad * 4;  // [Gpad][D + 8] bf16 (NT = 2 only)
   s.pre_off = round_up(s.q_off + Gpad * (D + 8) * 2, 16);
   s.bar_off = round_up(s.pre_off + (kMaxBatch + 1) * 4, 8);
   s.flag_off = s.bar_off + 2 * stages * 8;
@@ -125,19 +128,37 @@ __device__ inline int cta_of(long long t, long long T, int P) {
 
 __device__ inline int clamp_len(int len, int Lmax) { return len < 0 ? 0 : (len > Lmax ? Lmax : len); }
 
+// Consumer warp groups per CTA: with one n-tile per warp (G <= 8) a single
+// group leaves one consumer warp per SM sub-partition, whose per-tile
+// dependency chain then sets the pace; two groups on alternate tiles overlap
+// two chains.
+template <int NT>
+__host__ __device__ constexpr int tile_groups() { return NT == 1 ? 2 : 1; }
+
 template <int D, int NT>
-__global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
+__global__ void __launch_bounds__(288, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const Params p) {
   constexpr int KT = D / 16;  // 16-wide k-steps over D (QK) and m-tiles over D (PV)
+  constexpr int NG = tile_groups<NT>();
+  constexpr int KS = kKW * NG;  // key-slice states merged at the end of a piece
   const int Gpad = p.HS * 8 * NT;
-  const SmemLayout L = smem_layout<D>(p.stages, Gpad);
+  const SmemLayout L = smem_layout<D>(p.stages, Gpad, NG);
+  // Each tile group has a private ring of SG stages: tile i belongs to group
+  // i % NG and takes stage (i % NG) * SG + (i / NG) % SG.  A group therefore
+  // waits on use u of a stage only after it consumed use u - 1 itself, so a
+  // parity wait can never be satisfied by the phase before the one it wants
+  // (which could happen if two groups alternated on one stage and a load
+  // completed out of order).
+  const int SG = p.stages / NG;
+  auto stage_of = [&](long long i) { return (int)((i % NG) * SG + (i / NG) % SG); };
+  auto parity_of = [&](long long i) { return (uint32_t)(((i / NG) / SG) & 1); };
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* epi = reinterpret_cast<float*>(smem + L.epi_off);          // [KW][Gpad][D+4]
   float* red_m = reinterpret_cast<float*>(smem + L.red_off);        // [KW][Gpad]
-  float* red_l = red_m + kKW * Gpad;                                 // [KW][Gpad]
+  float* red_l = red_m + KS * Gpad;                                  // [KS][Gpad]
   int* pre = reinterpret_cast<int*>(smem + L.pre_off);               // [B+1]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + p.stages;
@@ -153,7 +174,7 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NC);
+      mbar_init(&empty[s], NC / NG);
     }
     *abort_flag = 0;
     *last_flag = 0;
@@ -223,9 +244,9 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
       long long issued = 0;
       for (long long t = s_c; t < e_c; ++t) {
         const int i = (int)(t - s_c);
-        const int s = i % p.stages;
-        if (i >= p.stages) {
-          if (!mbar_wait_bounded(&empty[s], ((i / p.stages) & 1) ^ 1, abort_flag, p.err)) break;
+        const int s = stage_of(i);
+        if (i / NG >= SG) {
+          if (!mbar_wait_bounded(&empty[s], parity_of(i) ^ 1, abort_flag, p.err)) break;
         }
         uint8_t* kdst = smem + s * L.stage_bytes;
         uint8_t* vdst = kdst + L.k_bytes;
@@ -240,10 +261,11 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
         iter_next(it, pre, B, Hkv);
       }
       // Wait (bounded) until every copy this thread issued has landed.
-      const long long first = issued > p.stages ? issued - p.stages : 0;
+      // The last NG * SG tiles hold the latest use of every stage.
+      const long long first = issued > NG * SG ? issued - NG * SG : 0;
       for (long long i = first; i < issued; ++i) {
         const unsigned long long t0 = globaltimer_ns();
-        while (!mbar_try_wait(&full[i % p.stages], (uint32_t)((i / p.stages) & 1))) {
+        while (!mbar_try_wait(&full[stage_of(i)], parity_of(i))) {
           if (globaltimer_ns() - t0 > kWaitLimitNs) {
             atomicOr(p.err, GQA_DEV_WAIT_TIMEOUT);
             break;
@@ -253,8 +275,11 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
     }
   } else {
     // ============================== consumers =============================
-    const int ks = warp % kKW;  // key slice
-    const int hs = warp / kKW;  // head slice
+    const int grp = warp / (kKW * p.HS);  // tile group: tiles i with i % NG == grp
+    const int wig = warp % (kKW * p.HS);
+    const int ks = wig % kKW;             // key slice
+    const int hs = wig / kKW;             // head slice
+    const int slice = grp * kKW + ks;     // index of this warp's state in the merge
     const int key0 = ks * 16;
     const int cthreads = NC * 32;
 
@@ -289,7 +314,7 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
     if (s_c < e_c) iter_seek(it, s_c, pre, B, Hkv);
     for (long long t = s_c; t < e_c; ++t) {
       const int i = (int)(t - s_c);
-      const int s = i % p.stages;
+      const int s = stage_of(i);
       const bool seg_first = (t == s_c) || (it.lt == 0);
       const bool seg_last = (t == e_c - 1) || (it.lt == it.nb - 1);
       const int pair = it.b * Hkv + it.j;
@@ -334,8 +359,9 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
         }
       }
 
-      if (live) live = mbar_wait_bounded(&full[s], (uint32_t)((i / p.stages) & 1), abort_flag, p.err);
-      if (live) {
+      const bool mine = (i % NG) == grp;
+      if (live && mine) live = mbar_wait_bounded(&full[s], parity_of(i), abort_flag, p.err);
+      if (live && mine) {
         const uint32_t kbase = smem_u32(smem + s * L.stage_bytes);
         const uint32_t vbase = kbase + L.k_bytes;
         const int valid = min(kBN, len_b - it.lt * kBN);  // >= 1
@@ -444,15 +470,15 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
             l += __shfl_xor_sync(0xffffffffu, l, 16);
             const int hg = (hs * NT + nt) * 8 + 2 * (lane & 3) + e;
             if ((lane >> 2) == 0) {
-              red_m[ks * Gpad + hg] = m_run[nt][e];
-              red_l[ks * Gpad + hg] = l;
+              red_m[slice * Gpad + hg] = m_run[nt][e];
+              red_l[slice * Gpad + hg] = l;
             }
           }
 #pragma unroll
           for (int mt = 0; mt < KT; ++mt) {
             const int d = mt * 16 + (lane >> 2);
             const int hg = (hs * NT + nt) * 8 + 2 * (lane & 3);
-            float* e0 = epi + (size_t)(ks * Gpad + hg) * (D + 4);
+            float* e0 = epi + (size_t)(slice * Gpad + hg) * (D + 4);
             float* e1 = e0 + (D + 4);
             e0[d] = acc[mt][nt][0];
             e1[d] = acc[mt][nt][1];
@@ -487,11 +513,11 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
         for (int h = tid; h < G; h += cthreads) {
           float M = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < kKW; ++k) M = fmaxf(M, red_m[k * Gpad + h]);
+          for (int k = 0; k < KS; ++k) M = fmaxf(M, red_m[k * Gpad + h]);
           const float Mu = M == -INFINITY ? 0.f : M;
           float Ls = 0.f;
 #pragma unroll
-          for (int k = 0; k < kKW; ++k) {
+          for (int k = 0; k < KS; ++k) {
             const float f = fast_exp2(red_m[k * Gpad + h] - Mu);
             Ls += f * red_l[k * Gpad + h];
             red_m[k * Gpad + h] = f;
@@ -504,7 +530,7 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
           const int h = e / (D / 4), d = 4 * (e % (D / 4));
           float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int k = 0; k < kKW; ++k) {
+          for (int k = 0; k < KS; ++k) {
             const float f = red_m[k * Gpad + h];
             const float4 x = *reinterpret_cast<const float4*>(epi + (size_t)(k * Gpad + h) * (D + 4) + d);
             acc4.x += f * x.x;
@@ -643,7 +669,7 @@ cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t s
   p.G = plan.G;
   p.Lmax = a.Lmax;
   p.HS = plan.HS;
-  p.NC = kKW * plan.HS;
+  p.NC = kKW * plan.HS * tile_groups<NT>();
   p.stages = plan.stages;
   p.num_ctas = plan.num_ctas;
   p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -674,14 +700,16 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
   plan->NT = NT;
   plan->HS = HS;
   plan->tile_keys = kBN;
-  plan->threads = 32 * (kKW * HS + 1);
+  const int NG = NT == 1 ? tile_groups<1>() : tile_groups<2>();
+  plan->threads = 32 * (kKW * HS * NG + 1);
   const long long tiles_max = (long long)B * Hkv * ((Lmax + kBN - 1) / kBN);
   plan->num_ctas = (int)std::min<long long>(tiles_max, std::min(kMaxCtas, std::max(1, sm_count)));
-  SmemLayout l0 = D == 64 ? smem_layout<64>(0, Gpad) : smem_layout<128>(0, Gpad);
-  const int stages = std::min(kMaxStages, (kSmemLimit - l0.total - 2 * kMaxStages * 8) / l0.stage_bytes);
-  if (stages < 2) return false;
+  SmemLayout l0 = D == 64 ? smem_layout<64>(0, Gpad, NG) : smem_layout<128>(0, Gpad, NG);
+  int stages = std::min(kMaxStages, (kSmemLimit - l0.total - 2 * kMaxStages * 8) / l0.stage_bytes);
+  stages = stages / NG * NG;  // every tile group gets a private ring of stages / NG
+  if (stages / NG < 2) return false;
   plan->stages = stages;
-  plan->smem_bytes = (size_t)(D == 64 ? smem_layout<64>(stages, Gpad) : smem_layout<128>(stages, Gpad)).total;
+  plan->smem_bytes = (size_t)(D == 64 ? smem_layout<64>(stages, Gpad, NG) : smem_layout<128>(stages, Gpad, NG)).total;
   plan->ws_part_floats = (size_t)plan->num_ctas * 2 * G * (D + 2);
   if (max_part_floats > 0 && plan->ws_part_floats > max_part_floats) return false;
   plan->chunk_tiles = 0;  // static split: one contiguous share per CTA
