@@ -40,6 +40,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -647,14 +649,56 @@ __global__ void __launch_bounds__(288, 1)
   __syncthreads();
 }
 
+// Tensor maps of recently used caches.  A map encodes only the base address,
+// shape and strides, so an entry with the same key is always valid (even if
+// the memory was freed and reallocated in between).  Serving loops call
+// decode with the same cache every step; this skips two driver encodes.
+struct TmapEntry {
+  const void* k;
+  const void* v;
+  int D, Lmax;
+  uint64_t pairs;
+  CUtensorMap tk, tv;
+};
+constexpr int kTmapCacheSize = 8;
+std::mutex g_tmap_mu;
+TmapEntry g_tmap_cache[kTmapCacheSize];
+int g_tmap_n = 0, g_tmap_next = 0;
+
+cudaError_t cache_tensor_maps(const DecodeArgs& a, int D, CUtensorMap* tk, CUtensorMap* tv) {
+  const uint64_t pairs = (uint64_t)a.B * a.Hkv;
+  std::lock_guard<std::mutex> lk(g_tmap_mu);
+  for (int e = 0; e < g_tmap_n; ++e) {
+    const TmapEntry& c = g_tmap_cache[e];
+    if (c.k == a.k_cache && c.v == a.v_cache && c.D == D && c.Lmax == a.Lmax && c.pairs == pairs) {
+      *tk = c.tk;
+      *tv = c.tv;
+      return cudaSuccess;
+    }
+  }
+  const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)a.Lmax * D * 2;
+  TmapEntry n;
+  n.k = a.k_cache;
+  n.v = a.v_cache;
+  n.D = D;
+  n.Lmax = a.Lmax;
+  n.pairs = pairs;
+  if (encode_tmap_bf16_3d(&n.tk, a.k_cache, D, a.Lmax, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS ||
+      encode_tmap_bf16_3d(&n.tv, a.v_cache, D, a.Lmax, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  g_tmap_cache[g_tmap_next] = n;
+  g_tmap_next = (g_tmap_next + 1) % kTmapCacheSize;
+  if (g_tmap_n < kTmapCacheSize) ++g_tmap_n;
+  *tk = n.tk;
+  *tv = n.tv;
+  return cudaSuccess;
+}
+
 template <int D, int NT>
 cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream) {
   CUtensorMap tmK, tmV;
-  const uint64_t pairs = (uint64_t)a.B * a.Hkv;
-  const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)a.Lmax * D * 2;
-  if (encode_tmap_bf16_3d(&tmK, a.k_cache, D, a.Lmax, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS ||
-      encode_tmap_bf16_3d(&tmV, a.v_cache, D, a.Lmax, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  cudaError_t e = cache_tensor_maps(a, D, &tmK, &tmV);
+  if (e != cudaSuccess) return e;
   Params p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.out = static_cast<__nv_bfloat16*>(a.out);
@@ -674,8 +718,16 @@ cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t s
   p.num_ctas = plan.num_ctas;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   auto kern = decode_kernel<D, NT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem_bytes);
-  if (e != cudaSuccess) return e;
+  // The opt-in shared-memory size is a per-device function attribute: set it
+  // once per device to the largest size any plan can ask for.
+  static std::atomic<unsigned long long> attr_set{0};  // bit d: set on device d (< 64)
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev >= 64 || !(attr_set.load() >> dev & 1ull)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set.fetch_or(1ull << dev);
+  }
   kern<<<plan.num_ctas, plan.threads, plan.smem_bytes, stream>>>(tmK, tmV, p);
   return cudaGetLastError();
 }

@@ -42,3 +42,36 @@ def test_piece_count_of_a_pair():
                 owners = {owner(t, T, P) for t in range(o, o + n)}
                 lo, hi = owner(o, T, P), owner(o + n - 1, T, P)
                 assert owners == set(range(lo, hi + 1))
+
+
+def stage_of(i, NG, SG):
+    """Stage of a CTA's i-th tile: tile group i % NG, private ring of SG stages."""
+    return (i % NG) * SG + (i // NG) % SG
+
+
+def parity_of(i, NG, SG):
+    return ((i // NG) // SG) & 1
+
+
+def test_tile_groups_never_share_a_stage():
+    """With NG consumer groups on alternate tiles, every stage is used by one
+    group only, its uses alternate in parity, and the producer's wait for a
+    free stage names the parity of that stage's previous use -- the property
+    that keeps a parity wait from being satisfied by an older phase."""
+    for NG, stages in [(1, 2), (1, 5), (1, 8), (2, 4), (2, 6), (2, 8)]:
+        SG = stages // NG
+        last = {}
+        for i in range(500):
+            s = stage_of(i, NG, SG)
+            assert 0 <= s < NG * SG
+            if s in last:
+                j = last[s]
+                assert j % NG == i % NG
+                assert (i // NG) - (j // NG) == SG        # the group's previous use
+                assert parity_of(j, NG, SG) == parity_of(i, NG, SG) ^ 1
+            else:
+                assert i // NG < SG                        # first use needs no wait
+            last[s] = i
+        # the producer's drain: the last NG*SG tiles cover every stage once
+        for issued in range(NG * SG, 60):
+            assert sorted(stage_of(i, NG, SG) for i in range(issued - NG * SG, issued)) == list(range(NG * SG))
