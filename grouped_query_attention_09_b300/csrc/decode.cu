@@ -738,6 +738,14 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
   if (B < 1 || B > kMaxBatch || Hkv < 1 || Hq % Hkv != 0 || Lmax < 1) return false;
   if (D != 64 && D != 128) return false;
   const int G = Hq / Hkv;
+  // Wide groups at D = 128 go to the tcgen05 kernel: its tensor core reads
+  // each K/V block from shared memory once for all G heads.
+  if (D == 128 && G >= 16 && G <= 128) {
+    if (!decode_tc_plan(B, Hq, Hkv, D, Lmax, sm_count, plan)) return false;
+    if (max_part_floats > 0 && plan->ws_part_floats > max_part_floats) return false;
+    return true;
+  }
+  plan->kind = 0;
   int Gpad, NT, HS;
   if (G <= 8) {
     Gpad = 8; NT = 1; HS = 1;
@@ -771,6 +779,7 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
 }
 
 cudaError_t decode_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream) {
+  if (plan.kind == 1) return decode_tc_launch(plan, a, stream);
   if (plan.D == 128) {
     return plan.NT == 1 ? launch_t<128, 1>(plan, a, stream) : launch_t<128, 2>(plan, a, stream);
   }

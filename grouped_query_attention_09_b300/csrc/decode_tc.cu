@@ -1,0 +1,692 @@
+// decode_tc.cu -- split-KV GQA decode on the tcgen05 tensor cores, for wide
+// groups (16 <= G <= 128 query heads per KV head, e.g. multi-query attention).
+//
+// Same computation as decode.cu: for every sequence b and query head h, the
+// new query attends to the first seqlens[b] rows of KV head j = h / G of the
+// bf16 [B, Hkv, Lmax, D] cache (the GQA paper notes on 51969.com, "分组查询
+// 注意力（GQA）"; the Huawei Cloud post "多头注意力机制的代码实现（MQA和GQA）",
+// section 5: scores q.k / sqrt(d), softmax, weighted sum of V).  With a wide
+// group the warp-level MMA path re-reads every K/V tile from shared memory once
+// per head slice; here the G query heads of a (b, j) pair are the M rows of one
+// tcgen05.mma (rows G..127 are padding and never read back), so each K/V block
+// crosses HBM once and shared memory once.
+//
+// Split ("Split-KV": the gsyq.cn page on xformers, "分块计算与内存优化"): the
+// flattened (b, j, 128-key block) space is cut into equal contiguous shares,
+// one per persistent CTA; a pair cut by share boundaries is merged by
+// log-sum-exp by the CTA that completes its last piece (arrival counter), as
+// in decode.cu, with the same workspace layout.
+//
+// Per block i of the share (warp roles, 256 threads):
+//   warp 0  TMA producer: the pair's Q tile [128 x D] once per piece (rows >=
+//           G are out of range and arrive as zeros), then K_i and V_i into a
+//           ring of 32 KiB stages.
+//   warp 1  TMEM owner and MMA issuer (all lanes walk the schedule, one
+//           elected lane issues): S_i = Q K_i^T into S buffer i % 2, then
+//           O += P_{i-1} V_{i-1} -- the next block's scores are computed while
+//           the softmax of the current one runs.
+//   warps 4-7  softmax and epilogue, one thread per query head (TMEM lane):
+//           mask keys past seqlens[b], running max (re-based only when it
+//           grows by more than 2^8), P = exp2(.) as bf16 over the S buffer,
+//           running sum; at the end of a piece, O / l to the output or the
+//           partial slot.  Warps whose 32 lanes are all padding rows skip the
+//           TMEM work but keep the barrier protocol.
+// TMEM: S buffers at columns [0, 128) and [128, 256), O at [256, 384).
+//
+// Every wait is bounded; on expiry GQA_DEV_WAIT_TIMEOUT is flagged, the roles
+// leave their loops, in-flight copies and MMAs are drained (bounded) and the
+// TMEM is freed.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tcgen05.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBN = 128;                      // keys per block
+constexpr int kBlockBytes = kBN * kD * 2;     // one K or V block: 32 KiB
+constexpr int kHalf = kBlockBytes / 2;        // one 64-column half (128-byte rows)
+constexpr int kQBytes = 128 * kD * 2;         // Q tile: 32 KiB
+constexpr int kThreads = 256;
+constexpr int kMaxBatch = 1024;
+constexpr int kMaxCtasTc = 160;
+constexpr int kSmemLimitTc = 232448;
+constexpr float kRebase = 8.0f;
+constexpr int kColO = 256;
+
+struct TcParams {
+  __nv_bfloat16* out;
+  const int32_t* seqlens;
+  float* part_acc;  // [num_ctas][2][G][D]
+  float* part_ml;   // [num_ctas][2][2][G]
+  int* counters;    // [B * Hkv]
+  unsigned* err;
+  int B, Hq, Hkv, G, Lmax, stages, num_ctas;
+  float scale_log2;
+};
+
+struct TcLayout {
+  int ring_off, pre_off, bar_off, misc_off, total;
+};
+
+__host__ __device__ inline TcLayout tc_layout(int stages) {
+  TcLayout l;
+  l.ring_off = kQBytes;
+  l.pre_off = l.ring_off + stages * kBlockBytes;
+  l.bar_off = l.pre_off + ((kMaxBatch + 1) * 4 + 7) / 8 * 8;
+  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done, o_full, mma_done
+  l.misc_off = l.bar_off + (2 + 2 * stages + 2 + 2 + 3) * 8;
+  l.total = l.misc_off + 4 * 40 + 1024;  // flags + scan scratch, + alignment slack
+  return l;
+}
+
+struct Iter {
+  int b, j, lt, nb;
+};
+
+__device__ inline void it_seek(Iter& it, long long t, const int* pre, int B, int Hkv) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)Hkv * pre[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  it.b = lo;
+  it.nb = pre[lo + 1] - pre[lo];
+  const long long r = t - (long long)Hkv * pre[lo];
+  it.j = (int)(r / it.nb);
+  it.lt = (int)(r % it.nb);
+}
+
+__device__ inline void it_next(Iter& it, const int* pre, int B, int Hkv) {
+  if (++it.lt < it.nb) return;
+  it.lt = 0;
+  if (++it.j < Hkv) return;
+  it.j = 0;
+  do { ++it.b; } while (it.b < B && pre[it.b + 1] == pre[it.b]);
+  it.nb = it.b < B ? pre[it.b + 1] - pre[it.b] : 0;
+}
+
+__device__ inline int owner_cta(long long t, long long T, int P) { return (int)(((t + 1) * P + T - 1) / T) - 1; }
+
+__device__ inline int clamp_seq(int len, int Lmax) { return len < 0 ? 0 : (len > Lmax ? Lmax : len); }
+
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity, unsigned* err) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, GQA_DEV_WAIT_TIMEOUT);
+      return;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+  const TcLayout L = tc_layout(p.stages);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_tile = smem;
+  uint8_t* ring = smem + L.ring_off;
+  int* pre = reinterpret_cast<int*>(smem + L.pre_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;
+  uint64_t* kv_empty = kv_full + p.stages;
+  uint64_t* s_full = kv_empty + p.stages;  // [2]
+  uint64_t* p_full = s_full + 2;           // [2]
+  uint64_t* o_done = p_full + 2;
+  uint64_t* o_full = o_done + 1;
+  uint64_t* mma_done = o_full + 1;
+  int* misc = reinterpret_cast<int*>(smem + L.misc_off);
+  volatile int* abort_flag = misc;
+  volatile int* merge_flag = misc + 1;
+  volatile int* chi_flag = misc + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 3);
+  int* scan = misc + 8;  // [8]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = p.B, Hkv = p.Hkv, G = p.G;
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&s_full[k], 1);
+      mbar_init(&p_full[k], 128);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(o_full, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+
+  // ---- blocks per sequence and their exclusive prefix pre[0..B]
+  {
+    const int per = (B + kThreads - 1) / kThreads;
+    const int lo = tid * per, hi = min(B, lo + per);
+    int local = 0;
+    unsigned flags = 0;
+    for (int i = lo; i < hi; ++i) {
+      const int len = p.seqlens[i];
+      if (len > p.Lmax) flags |= GQA_DEV_SEQLEN_CLAMPED;
+      if (len <= 0) flags |= GQA_DEV_EMPTY_CONTEXT;
+      local += (clamp_seq(len, p.Lmax) + kBN - 1) / kBN;
+    }
+    if (flags && blockIdx.x == 0) atomicOr(p.err, flags);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) scan[warp] = incl;
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) {
+      const int w = lane < kThreads / 32 ? scan[lane] : 0;
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += v;
+      }
+      if (lane < kThreads / 32) scan[lane] = wi - w;
+    }
+    __syncthreads();
+    int run = scan[warp] + incl - local;
+    for (int i = lo; i < hi; ++i) {
+      pre[i] = run;
+      run += (clamp_seq(p.seqlens[i], p.Lmax) + kBN - 1) / kBN;
+    }
+    if (lo < B && hi == B) pre[B] = run;
+  }
+  __syncthreads();
+  const uint32_t tmem = *tmem_slot;
+
+  const long long T = (long long)Hkv * pre[B];
+  const int P = (int)(T < p.num_ctas ? T : p.num_ctas);
+  const bool active = (int)blockIdx.x < P;
+  const long long s_c = active ? T * blockIdx.x / P : 0;
+  const long long e_c = active ? T * (blockIdx.x + 1) / P : 0;
+
+  // Zero the outputs of sequences with an empty context.
+  for (int b = blockIdx.x; b < B; b += p.num_ctas) {
+    if (pre[b + 1] != pre[b]) continue;
+    __nv_bfloat16* o = p.out + (size_t)b * p.Hq * kD;
+    for (int e = tid; e < p.Hq * kD; e += kThreads) o[e] = __float2bfloat16_rn(0.f);
+  }
+
+  auto kslot = [&](long long i) { return (int)((2 * i) % p.stages); };
+  auto kpar = [&](long long i) { return (uint32_t)(((2 * i) / p.stages) & 1); };
+  auto vslot = [&](long long i) { return (int)((2 * i + 1) % p.stages); };
+  auto vpar = [&](long long i) { return (uint32_t)(((2 * i + 1) / p.stages) & 1); };
+
+  if (warp == 0) {
+    // ================================================================ producer
+    if (lane == 0 && s_c < e_c) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const uint64_t pol = l2_policy_evict_first();
+      Iter it;
+      it_seek(it, s_c, pre, B, Hkv);
+      int seg = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (long long t = s_c; t < e_c && ok; ++t) {
+        const long long i = t - s_c;
+        const int z = it.b * Hkv + it.j;
+        if (t == s_c || it.lt == 0) {
+          ok = mbar_wait_bounded(q_empty, (seg & 1) ^ 1, abort_flag, p.err);
+          if (!ok) break;
+          mbar_arrive_expect_tx(q_full, kQBytes);
+          tma_load_3d(q_tile, &tmQ, 0, 0, z, q_full, pol);
+          tma_load_3d(q_tile + kHalf, &tmQ, 64, 0, z, q_full, pol);
+          ++seg;
+        }
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          const int s = kv ? vslot(i) : kslot(i);
+          const uint32_t par = kv ? vpar(i) : kpar(i);
+          if (2 * i + kv >= p.stages) {
+            ok = mbar_wait_bounded(&kv_empty[s], par ^ 1, abort_flag, p.err);
+            if (!ok) break;
+          }
+          uint8_t* dst = ring + s * kBlockBytes;
+          const CUtensorMap* m = kv ? &tmV : &tmK;
+          mbar_arrive_expect_tx(&kv_full[s], kBlockBytes);
+          tma_load_3d(dst, m, 0, it.lt * kBN, z, &kv_full[s], pol);
+          tma_load_3d(dst + kHalf, m, 64, it.lt * kBN, z, &kv_full[s], pol);
+          issued = 2 * i + kv + 1;
+        }
+        it_next(it, pre, B, Hkv);
+      }
+      // Drain: the last `stages` loads hold the latest use of every slot.
+      for (long long n = issued > p.stages ? issued - p.stages : 0; n < issued; ++n)
+        wait_drain(&kv_full[n % p.stages], (uint32_t)((n / p.stages) & 1), p.err);
+      if (seg > 0) wait_drain(q_full, (seg - 1) & 1, p.err);
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA
+    constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kBN, false);
+    constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, kD, true);
+    const bool leader = elect_one_sync();
+    const uint64_t dq = tc::sdesc_sw128(smem_u32(q_tile), 16, 1024);
+    const uint64_t dk = tc::sdesc_sw128(smem_u32(ring), 16, 1024);
+    const uint64_t dv = tc::sdesc_sw128(smem_u32(ring), kHalf, 1024);
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      const bool w = mbar_wait_bounded(bar, parity, abort_flag, p.err);
+      return __all_sync(0xffffffffu, w);
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (leader) tc::commit(bar);
+    };
+    auto issue_s = [&](long long i) {
+      const uint64_t b0 = dk + (uint64_t)((kslot(i) * kBlockBytes) >> 4);
+      const uint32_t d = tmem + (uint32_t)(i & 1) * 128;
+      if (leader) {
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k) {
+          const uint64_t off = (uint64_t)(((k >> 2) * kHalf + (k & 3) * 32) >> 4);
+          tc::mma_ss(d, dq + off, b0 + off, idesc_s, k > 0);
+        }
+      }
+    };
+    auto issue_pv = [&](long long i, bool acc) {
+      const uint64_t b0 = dv + (uint64_t)((vslot(i) * kBlockBytes) >> 4);
+      const uint32_t a = tmem + (uint32_t)(i & 1) * 128;
+      if (leader) {
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)
+          tc::mma_ts(tmem + kColO, a + k * 8, b0 + (uint64_t)((k * 16 * 128) >> 4), idesc_o, (acc || k > 0) ? 1u : 0u);
+      }
+    };
+    Iter it;
+    if (s_c < e_c) it_seek(it, s_c, pre, B, Hkv);
+    int seg = 0;
+    bool ok = true;
+    bool prev_first = false, prev_last = false;
+    for (long long t = s_c; t < e_c && ok; ++t) {
+      const long long i = t - s_c;
+      const bool first = (t == s_c) || it.lt == 0;
+      const bool last = (t == e_c - 1) || it.lt == it.nb - 1;
+      if (first) {
+        ok = wait(q_full, seg & 1);
+        if (!ok) break;
+        ++seg;
+      }
+      ok = wait(&kv_full[kslot(i)], kpar(i));
+      if (!ok) break;
+      tc::fence_after_sync();
+      issue_s(i);
+      commit(&s_full[i & 1]);
+      commit(&kv_empty[kslot(i)]);
+      if (last) commit(q_empty);
+      if (i > 0) {
+        // P V of the previous block (its scores were signalled one block ago)
+        ok = wait(&p_full[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1));
+        if (!ok) break;
+        ok = wait(&kv_full[vslot(i - 1)], vpar(i - 1));
+        if (!ok) break;
+        tc::fence_after_sync();
+        issue_pv(i - 1, !prev_first);
+        commit(&kv_empty[vslot(i - 1)]);
+        commit(o_done);
+        if (prev_last) commit(o_full);
+      }
+      prev_first = first;
+      prev_last = last;
+      it_next(it, pre, B, Hkv);
+    }
+    if (ok && e_c > s_c) {
+      const long long i = e_c - s_c;  // P V of the share's last block
+      ok = wait(&p_full[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1));
+      if (ok) ok = wait(&kv_full[vslot(i - 1)], vpar(i - 1));
+      if (ok) {
+        tc::fence_after_sync();
+        issue_pv(i - 1, !prev_first);
+        commit(&kv_empty[vslot(i - 1)]);
+        commit(o_done);
+        commit(o_full);
+      }
+    }
+    commit(mma_done);
+    wait_drain(mma_done, 0, p.err);
+  } else if (warp >= 4) {
+    // ================================================================ softmax + epilogue
+    const int r = tid - 128;                 // query head within the group = TMEM lane
+    const int wq = warp - 4;                 // lane quarter
+    const bool rows = wq * 32 < G;           // this warp holds at least one real head
+    const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+    const uint32_t o_tm = tmem + lane_addr + kColO;
+    Iter it;
+    if (s_c < e_c) it_seek(it, s_c, pre, B, Hkv);
+    int seg = 0, seg_lt0 = 0, len_b = 0;
+    float m_use = -INFINITY, l = 0.f;
+    // After a timeout the group keeps walking the share with every wait
+    // returning at once (the abort flag is up), so that all four warps always
+    // meet the same named barriers; only the memory work is skipped.
+    bool ok = true;
+    for (long long t = s_c; t < e_c; ++t) {
+      const long long i = t - s_c;
+      const bool first = (t == s_c) || it.lt == 0;
+      const bool last = (t == e_c - 1) || it.lt == it.nb - 1;
+      if (first) {
+        seg_lt0 = it.lt;
+        len_b = clamp_seq(p.seqlens[it.b], p.Lmax);
+        m_use = -INFINITY;
+        l = 0.f;
+      }
+      const int valid = min(kBN, len_b - it.lt * kBN);  // keys of this block that exist (>= 1)
+      {
+        const bool w = mbar_wait_bounded(&s_full[i & 1], (uint32_t)((i >> 1) & 1), abort_flag, p.err);
+        ok = __all_sync(0xffffffffu, w) && ok;
+      }
+      tc::fence_after_sync();
+      const uint32_t s_tm = tmem + lane_addr + (uint32_t)(i & 1) * 128;
+      if (rows && ok) {
+        uint32_t s[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::ld_32x32b_x32(s_tm + c * 32, s[c]);
+        tc::wait_ld_regs(s[0]);
+        tc::pin_regs(s[1]);
+        tc::pin_regs(s[2]);
+        tc::pin_regs(s[3]);
+        if (valid < kBN) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e >= valid) s[c][e] = __float_as_uint(-INFINITY);
+        }
+        float mxv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float m = fmax3(__uint_as_float(s[0][e]), __uint_as_float(s[0][e + 8]), __uint_as_float(s[0][e + 16]));
+          m = fmaxf(m, __uint_as_float(s[0][e + 24]));
+#pragma unroll
+          for (int c = 1; c < 4; ++c)
+            m = fmax3(m, fmaxf(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 8])),
+                      fmaxf(__uint_as_float(s[c][e + 16]), __uint_as_float(s[c][e + 24])));
+          mxv[e] = m;
+        }
+        const float mx = fmaxf(fmax3(mxv[0], mxv[1], mxv[2]), fmax3(fmax3(mxv[3], mxv[4], mxv[5]), mxv[6], mxv[7]));
+        const float mxs = mx * p.scale_log2;
+        const bool rebase = mxs > m_use + kRebase;
+        const bool any_rebase = __any_sync(0xffffffffu, rebase);
+        const float m_new = rebase ? mxs : m_use;
+        const float alpha = rebase ? fast_exp2(m_use - m_new) : 1.f;
+        m_use = m_new;
+        const float ref = m_use == -INFINITY ? 0.f : m_use;
+        const float sl = p.scale_log2, nref = -ref;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pw[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float x0, x1;
+            fma2(x0, x1, __uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1]), sl, sl, nref, nref);
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            ls[e & 3] += p0 + p1;
+            pw[e] = pack_bf16x2(p0, p1);
+          }
+          tc::st_32x32b_x16(s_tm + c * 16, pw);
+        }
+        l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+        if (any_rebase && !first) {
+          // O holds blocks up to i - 1: wait for that P V, then re-base it.
+          const bool w = mbar_wait_bounded(o_done, (uint32_t)((i - 1) & 1), abort_flag, p.err);
+          if (__all_sync(0xffffffffu, w)) {
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[32];
+              tc::ld_32x32b_x32(o_tm + c * 32, o);
+              tc::wait_ld_regs(o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tc::st_32x32b_x32(o_tm + c * 32, o);
+            }
+          }
+        }
+        tc::wait_st();
+      }
+      if (valid < kBN) {
+        // Cache rows at and past seqlens[b] may hold anything (NaN included):
+        // zero them in the V block so that P = 0 there contributes exactly 0.
+        uint8_t* vb = ring + vslot(i) * kBlockBytes;
+        const bool w = mbar_wait_bounded(&kv_full[vslot(i)], vpar(i), abort_flag, p.err);
+        ok = __all_sync(0xffffffffu, w) && ok;
+        if (ok) {
+          const int nchunks = (kBN - valid) * 16;  // 16-byte chunks over both halves
+          for (int e = r; e < nchunks; e += 128) {
+            const int row = valid + (e >> 4), rem = e & 15;
+            *reinterpret_cast<uint4*>(vb + (rem >> 3) * kHalf + row * 128 + (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+      }
+      tc::fence_before_sync();
+      mbar_arrive(&p_full[i & 1]);
+
+      if (last) {
+        // ---- end of a piece: O / l to the output, or a partial for the merge
+        {
+          const bool w = mbar_wait_bounded(o_full, (uint32_t)(seg & 1), abort_flag, p.err);
+          ok = __all_sync(0xffffffffu, w) && ok;
+        }
+        ++seg;
+        tc::fence_after_sync();
+        const bool complete = (seg_lt0 == 0) && (it.lt == it.nb - 1);
+        const int slot = seg_lt0 == 0 ? 1 : 0;
+        const size_t slot_idx = (size_t)blockIdx.x * 2 + slot;
+        __nv_bfloat16* outp = p.out + ((size_t)it.b * p.Hq + (size_t)it.j * G) * kD;
+        if (rows && ok) {
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tc::ld_32x32b_x32(o_tm + c * 32, o);
+            tc::wait_ld_regs(o);
+            if (r < G) {
+              if (complete) {
+                uint4* dst = reinterpret_cast<uint4*>(outp + (size_t)r * kD + c * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  uint32_t w[4];
+#pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(o[v * 8 + 2 * e]) * inv, __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
+                  dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+              } else {
+                float4* dst = reinterpret_cast<float4*>(p.part_acc + (slot_idx * G + r) * kD + c * 32);
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                  dst[v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                       __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+              }
+            }
+          }
+          if (!complete && r < G) {
+            p.part_ml[(slot_idx * 2 + 0) * G + r] = m_use;
+            p.part_ml[(slot_idx * 2 + 1) * G + r] = l;
+          }
+        }
+        tc::fence_before_sync();
+        if (!complete) {
+          // Publish the piece; the CTA that brings the pair's count to its
+          // number of pieces merges them all.
+          named_bar_sync(1, 128);
+          if (r == 0 && !*abort_flag) {
+            const long long o_p = (long long)Hkv * pre[it.b] + (long long)it.j * it.nb;
+            const int c_lo = owner_cta(o_p, T, P);
+            const int c_hi = owner_cta(o_p + it.nb - 1, T, P);
+            __threadfence();
+            const int pair = it.b * Hkv + it.j;
+            const int old = atomicAdd(&p.counters[pair], 1);
+            const bool lastc = old == c_hi - c_lo;
+            if (lastc) {
+              p.counters[pair] = 0;  // ready for the next call
+              __threadfence();
+            }
+            *merge_flag = lastc ? c_lo + 1 : 0;
+            *chi_flag = c_hi;
+          } else if (r == 0) {
+            *merge_flag = 0;
+          }
+          named_bar_sync(1, 128);
+          const int lf = *merge_flag;
+          if (lf) {
+            // Merge all pieces of the pair.  Thread r covers head h0 + r / 4
+            // and columns [32 (r % 4), 32 (r % 4) + 32): one pass for the
+            // pieces' maxima, one for the weighted sums, with the loads of
+            // consecutive pieces in flight together.
+            const int c_lo = lf - 1, nseg = *chi_flag - c_lo + 1;
+            for (int h0 = 0; h0 < G; h0 += 32) {
+              const int h = h0 + (r >> 2), cg = r & 3;
+              if (h < G) {
+                float M = -INFINITY;
+#pragma unroll 4
+                for (int s2 = 0; s2 < nseg; ++s2) {
+                  const size_t si = (size_t)(c_lo + s2) * 2 + (s2 == 0 ? 1 : 0);
+                  M = fmaxf(M, __ldcg(p.part_ml + (si * 2 + 0) * G + h));
+                }
+                const float Mu = M == -INFINITY ? 0.f : M;
+                float Ls = 0.f;
+                float4 acc4[8];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) acc4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+                for (int s2 = 0; s2 < nseg; ++s2) {
+                  const size_t si = (size_t)(c_lo + s2) * 2 + (s2 == 0 ? 1 : 0);
+                  const float f = fast_exp2(__ldcg(p.part_ml + (si * 2 + 0) * G + h) - Mu);
+                  Ls += f * __ldcg(p.part_ml + (si * 2 + 1) * G + h);
+                  const float4* src = reinterpret_cast<const float4*>(p.part_acc + (si * G + h) * kD + cg * 32);
+#pragma unroll
+                  for (int v = 0; v < 8; ++v) {
+                    const float4 x = __ldcg(src + v);
+                    acc4[v].x += f * x.x;
+                    acc4[v].y += f * x.y;
+                    acc4[v].z += f * x.z;
+                    acc4[v].w += f * x.w;
+                  }
+                }
+                const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+                uint4* dst = reinterpret_cast<uint4*>(outp + (size_t)h * kD + cg * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  const float4 a0 = acc4[2 * v], a1 = acc4[2 * v + 1];
+                  dst[v] = make_uint4(pack_bf16x2(a0.x * inv, a0.y * inv), pack_bf16x2(a0.z * inv, a0.w * inv),
+                                      pack_bf16x2(a1.x * inv, a1.y * inv), pack_bf16x2(a1.z * inv, a1.w * inv));
+                }
+              }
+            }
+          }
+          named_bar_sync(1, 128);
+        }
+      }
+      it_next(it, pre, B, Hkv);
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool decode_tc_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan) {
+  if (B < 1 || B > kMaxBatch || Hkv < 1 || Hq % Hkv != 0 || Lmax < 1 || D != kD) return false;
+  const int G = Hq / Hkv;
+  if (G < 1 || G > 128) return false;
+  plan->kind = 1;
+  plan->D = D;
+  plan->G = G;
+  plan->Gpad = 128;
+  plan->NT = 0;
+  plan->HS = 0;
+  plan->tile_keys = kBN;
+  plan->threads = kThreads;
+  const long long blocks_max = (long long)B * Hkv * ((Lmax + kBN - 1) / kBN);
+  plan->num_ctas = (int)std::min<long long>(blocks_max, std::min(kMaxCtasTc, std::max(1, sm_count)));
+  const TcLayout l0 = tc_layout(0);
+  int stages = (kSmemLimitTc - l0.total - 16 * 8) / kBlockBytes;
+  stages = std::min(stages, 8);
+  if (stages < 2) return false;
+  plan->stages = stages;
+  plan->smem_bytes = (size_t)tc_layout(stages).total;
+  plan->ws_part_floats = (size_t)plan->num_ctas * 2 * G * (D + 2);
+  plan->chunk_tiles = 0;
+  plan->chunks_max = plan->num_ctas;
+  plan->ws_counters = (size_t)B * Hkv;
+  return true;
+}
+
+cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  const uint64_t pairs = (uint64_t)a.B * a.Hkv;
+  const int G = plan.G;
+  // Q viewed as [B * Hkv][G][D]: a 128-row box starting at row 0 reads the
+  // group's G heads and zero-fills rows G..127.
+  if (encode_tmap_bf16_3d(&tq, a.q, kD, (uint64_t)G, pairs, (uint64_t)kD * 2, (uint64_t)G * kD * 2, 64, 128, 1) !=
+          CUDA_SUCCESS ||
+      encode_tmap_bf16_3d(&tk, a.k_cache, kD, a.Lmax, pairs, (uint64_t)kD * 2, (uint64_t)a.Lmax * kD * 2, 64, kBN,
+                          1) != CUDA_SUCCESS ||
+      encode_tmap_bf16_3d(&tv, a.v_cache, kD, a.Lmax, pairs, (uint64_t)kD * 2, (uint64_t)a.Lmax * kD * 2, 64, kBN,
+                          1) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  TcParams p;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.seqlens = a.seqlens;
+  p.part_acc = a.ws_part;
+  p.part_ml = a.ws_part + (size_t)plan.num_ctas * 2 * G * kD;
+  p.counters = a.ws_counters;
+  p.err = a.err;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = G;
+  p.Lmax = a.Lmax;
+  p.stages = plan.stages;
+  p.num_ctas = plan.num_ctas;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  static std::atomic<unsigned long long> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !(attr_set.load() >> dev & 1ull)) {
+    e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimitTc);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set.fetch_or(1ull << dev);
+  }
+  decode_tc_kernel<<<plan.num_ctas, kThreads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa

@@ -15,6 +15,7 @@ CUresult encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t dim0, 
 
 // ------------------------------------------------------------------ decode
 struct DecodePlan {
+  int kind;                // 0: warp-level MMA kernel (decode.cu), 1: tcgen05 kernel (decode_tc.cu)
   int D, G, Gpad, NT, HS;  // head dim, group size, padded group, n-tiles/warp, head slices
   int tile_keys;           // keys per pipeline tile
   int chunk_tiles;         // tiles per scheduling chunk (unit of work a CTA claims)
@@ -48,6 +49,11 @@ struct DecodeArgs {
 };
 
 cudaError_t decode_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream);
+
+// The tcgen05 decode for wide groups (D = 128, 1 <= G <= 128); decode_plan
+// routes G >= 16 to it.  Same workspace layout as the warp-level kernel.
+bool decode_tc_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan);
+cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream);
 
 // ------------------------------------------------------------------ prefill
 struct PrefillArgs {

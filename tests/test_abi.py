@@ -81,17 +81,19 @@ def test_host_entry_points_validate_first(gqa_lib):
     assert lib.gqa_prefill_host(P, P, P, P, 1, 16, 4, 2, 96, 1, None) == 2
 
 
-@pytest.mark.parametrize("shape,ctas", [
-    ((2, 8, 2, 64, 128), 8),          # 4 (b, kv head) pairs x 2 tiles of 64 keys
-    ((16, 32, 8, 128, 4096), 148),
-    ((8, 64, 8, 128, 16384), 148),
-    ((64, 32, 1, 128, 2048), 148),
+@pytest.mark.parametrize("shape,tile_keys,ctas", [
+    ((2, 8, 2, 64, 128), 64, 8),          # 4 (b, kv head) pairs x 2 tiles of 64 keys
+    ((16, 32, 8, 128, 4096), 64, 148),
+    ((8, 64, 8, 128, 16384), 64, 148),
+    ((64, 32, 1, 128, 2048), 128, 148),   # G = 32: tcgen05 kernel, 128-key blocks
+    ((2, 32, 1, 128, 300), 128, 6),       # 2 pairs x 3 blocks
 ])
-def test_decode_plan(gqa_lib, shape, ctas):
-    """Split plan: 64-key tiles; at most one persistent CTA per SM (148 on a
-    B300) and never more CTAs than tiles."""
+def test_decode_plan(gqa_lib, shape, tile_keys, ctas):
+    """Split plan: 64-key tiles for G <= 8 (warp-level MMA kernel), 128-key
+    blocks for wide groups at D = 128 (tcgen05 kernel); at most one persistent
+    CTA per SM (148 on a B300) and never more CTAs than tiles."""
     tile, n = gqa_lib.gqa_decode_plan(*shape)
-    assert tile == 64
+    assert tile == tile_keys
     assert n == ctas
 
 

@@ -136,3 +136,50 @@ def test_side_stream_and_host_entry_point(gqa_lib, cuda_device):
     assert torch.equal(ref, other)
     host = gqa_lib.gqa_decode_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), sl.pin_memory())
     assert torch.equal(ref.cpu(), host)
+
+
+# ---- wide groups (G >= 16 at D = 128): the tcgen05 decode kernel
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,lens", [
+    (3, 16, 1, 700, [700, 129, 1]),          # G = 16; one key; one past a block edge
+    (2, 24, 1, 400, [400, 255]),             # G = 24 (not a power of two)
+    (2, 64, 1, 1000, [1000, 513]),           # G = 64: two warps of heads
+    (1, 128, 1, 384, [384]),                 # G = 128: every TMEM lane a head
+    (4, 64, 2, 900, [900, 128, 127, 640]),   # G = 32, two KV heads; block-exact lengths
+])
+def test_wide_group_shapes(gqa_lib, oracle_mod, cuda_device, B, Hq, Hkv, Lmax, lens):
+    w = W.DecodeWorkload("wide", B, Hq, Hkv, 128, Lmax, 1, Lmax, 2000 + B * Hq + Lmax)
+    q, k, v, _ = W.make_decode_inputs(w)
+    sl = torch.tensor(lens, dtype=torch.int32)
+    out, flags = run_decode(gqa_lib, q, k, v, sl, w.scale, cuda_device)
+    assert flags == 0
+    assert_parity(out, oracle_decode(oracle_mod, q, k, v, sl, w.scale), f"wide {B},{Hq},{Hkv},{lens}")
+
+
+def test_wide_group_nan_tail_peaky_and_edges(gqa_lib, oracle_mod, cuda_device):
+    """G = 32: NaN-poisoned cache tail, peaky q (x8), an empty context and a
+    clamped length in one batch."""
+    w = W.DecodeWorkload("wide_edges", 6, 32, 1, 128, 1024, 1, 1024, 91)
+    q, k, v, _ = W.make_decode_inputs(w, q_mult=8.0)
+    sl = torch.tensor([1024, 1, 700, 0, 5000, 333], dtype=torch.int32)
+    W.poison_tail(k, v, sl.clamp(max=1024))
+    out, flags = run_decode(gqa_lib, q, k, v, sl, w.scale, cuda_device)
+    assert flags == (gqa_lib.GQA_DEV_EMPTY_CONTEXT | gqa_lib.GQA_DEV_SEQLEN_CLAMPED)
+    assert np.all(out[3] == 0)
+    ref = oracle_decode(oracle_mod, q, k, v, sl.clamp(min=1, max=1024), w.scale)
+    keep = [0, 1, 2, 4, 5]
+    assert_parity(out[keep], ref[keep], "wide edges")
+
+
+def test_wide_group_many_short_sequences_and_repeat(gqa_lib, oracle_mod, cuda_device):
+    """Many short MQA sequences (most pieces complete inside one CTA), twice in
+    a row: identical bits, counters back at zero."""
+    w = W.DecodeWorkload("wide_short", 300, 32, 1, 128, 300, 1, 300, 93)
+    q, k, v, sl = W.make_decode_inputs(w)
+    qd, kd, vd, sld = q.to(cuda_device), k.to(cuda_device), v.to(cuda_device), sl.to(cuda_device)
+    a = gqa_lib.gqa_decode(qd, kd, vd, sld).clone()
+    b = gqa_lib.gqa_decode(qd, kd, vd, sld)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert gqa_lib.gqa_get_device_status() == 0
+    assert_parity(a.double().cpu().numpy(), oracle_decode(oracle_mod, q, k, v, sl, w.scale), "wide short")
