@@ -764,6 +764,15 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
   plan->threads = 32 * (kKW * HS * NG + 1);
   const long long tiles_max = (long long)B * Hkv * ((Lmax + kBN - 1) / kBN);
   plan->num_ctas = (int)std::min<long long>(tiles_max, std::min(kMaxCtas, std::max(1, sm_count)));
+  {
+    // One CTA per (b, kv head) pair when the pairs nearly fill the GPU: with
+    // equal lengths every share is then exactly one pair, so no pair is cut
+    // and no cross-CTA merge runs (each SM's ring still keeps its share of
+    // HBM bandwidth in flight).  Ragged lengths are still balanced by the
+    // tile split, at the cost of some cuts.
+    const long long pairs = (long long)B * Hkv;
+    if (pairs <= plan->num_ctas && pairs * 4 >= (long long)plan->num_ctas * 3) plan->num_ctas = (int)pairs;
+  }
   SmemLayout l0 = D == 64 ? smem_layout<64>(0, Gpad, NG) : smem_layout<128>(0, Gpad, NG);
   int stages = std::min(kMaxStages, (kSmemLimit - l0.total - 2 * kMaxStages * 8) / l0.stage_bytes);
   stages = stages / NG * NG;  // every tile group gets a private ring of stages / NG

@@ -83,7 +83,7 @@ def test_host_entry_points_validate_first(gqa_lib):
 
 @pytest.mark.parametrize("shape,tile_keys,ctas", [
     ((2, 8, 2, 64, 128), 64, 8),          # 4 (b, kv head) pairs x 2 tiles of 64 keys
-    ((16, 32, 8, 128, 4096), 64, 148),
+    ((16, 32, 8, 128, 4096), 64, 128),    # 128 pairs nearly fill 148 SMs: one CTA per pair
     ((8, 64, 8, 128, 16384), 64, 148),
     ((64, 32, 1, 128, 2048), 128, 148),   # G = 32: tcgen05 kernel, 128-key blocks
     ((2, 32, 1, 128, 300), 128, 6),       # 2 pairs x 3 blocks
@@ -91,7 +91,8 @@ def test_host_entry_points_validate_first(gqa_lib):
 def test_decode_plan(gqa_lib, shape, tile_keys, ctas):
     """Split plan: 64-key tiles for G <= 8 (warp-level MMA kernel), 128-key
     blocks for wide groups at D = 128 (tcgen05 kernel); at most one persistent
-    CTA per SM (148 on a B300) and never more CTAs than tiles."""
+    CTA per SM (148 on a B300), never more CTAs than tiles, and one CTA per
+    (b, kv head) pair when the pairs fill at least three quarters of the SMs."""
     tile, n = gqa_lib.gqa_decode_plan(*shape)
     assert tile == tile_keys
     assert n == ctas
