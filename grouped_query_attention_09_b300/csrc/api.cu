@@ -279,7 +279,7 @@ const char* gqa_status_string(int status) {
   switch (status) {
     case GQA_OK: return "GQA_OK";
     case GQA_ERR_INVALID_ARG: return "GQA_ERR_INVALID_ARG: a size is <= 0, Hq % Hkv != 0, causal is not 0/1 or scale is not finite and > 0";
-    case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED: shape not implemented (decode: D in {64,128}, Hq/Hkv <= 8, 16 or 32, B <= 1024; prefill: D == 128)";
+    case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED: shape not implemented (decode: D = 128 with Hq/Hkv <= 128, or D = 64 with Hq/Hkv <= 8, 16 or 32; B <= 1024; prefill: D == 128)";
     case GQA_ERR_NULL: return "GQA_ERR_NULL: a required pointer is NULL";
     case GQA_ERR_MISALIGNED: return "GQA_ERR_MISALIGNED: tensor pointers must be 16-byte aligned (seqlens 4-byte)";
     case GQA_ERR_CUDA: {

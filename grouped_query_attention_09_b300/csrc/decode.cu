@@ -740,7 +740,7 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
   const int G = Hq / Hkv;
   // Wide groups at D = 128 go to the tcgen05 kernel: its tensor core reads
   // each K/V block from shared memory once for all G heads.
-  if (D == 128 && G >= 16 && G <= 128) {
+  if (D == 128 && G > 8 && G <= 128) {
     if (!decode_tc_plan(B, Hq, Hkv, D, Lmax, sm_count, plan)) return false;
     if (max_part_floats > 0 && plan->ws_part_floats > max_part_floats) return false;
     return true;

@@ -51,7 +51,7 @@ struct DecodeArgs {
 cudaError_t decode_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream);
 
 // The tcgen05 decode for wide groups (D = 128, 1 <= G <= 128); decode_plan
-// routes G >= 16 to it.  Same workspace layout as the warp-level kernel.
+// routes G > 8 to it.  Same workspace layout as the warp-level kernel.
 bool decode_tc_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan);
 cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream);
 

@@ -81,8 +81,10 @@ typedef enum gqa_status {
  * seqlens[b] > Lmax is clamped to Lmax; seqlens[b] <= 0 gives a zero output
  * row; both set a device status bit.
  *
- * Supported: D in {64, 128}; G = Hq/Hkv in {1..8, 16, 32};
- * 1 <= B <= 1024.  Otherwise GQA_ERR_UNSUPPORTED.
+ * Supported: D = 128 with 1 <= G <= 128 (G = Hq/Hkv); D = 64 with G in
+ * {1..8, 16, 32}; 1 <= B <= 1024.  Otherwise GQA_ERR_UNSUPPORTED.  G <= 8
+ * (and D = 64) runs a warp-level MMA kernel; wider groups at D = 128 run a
+ * tcgen05 kernel with the group's heads as the rows of each MMA.
  *
  * Work is split across a persistent grid: the (b, j, key-tile) space is cut
  * into equal contiguous shares, one per CTA (split-KV, the gsyq.cn page on

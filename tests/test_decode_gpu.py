@@ -143,6 +143,7 @@ def test_side_stream_and_host_entry_point(gqa_lib, cuda_device):
 @pytest.mark.parametrize("B,Hq,Hkv,Lmax,lens", [
     (3, 16, 1, 700, [700, 129, 1]),          # G = 16; one key; one past a block edge
     (2, 24, 1, 400, [400, 255]),             # G = 24 (not a power of two)
+    (3, 36, 3, 260, [260, 1, 200]),          # G = 12 (between the two kernels' ranges)
     (2, 64, 1, 1000, [1000, 513]),           # G = 64: two warps of heads
     (1, 128, 1, 384, [384]),                 # G = 128: every TMEM lane a head
     (4, 64, 2, 900, [900, 128, 127, 640]),   # G = 32, two KV heads; block-exact lengths
