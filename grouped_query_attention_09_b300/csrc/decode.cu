@@ -557,19 +557,15 @@ __global__ void __launch_bounds__(288, 1)
 
         if (!complete) {
           // Publish this piece: the barrier orders every thread's partial
-          // stores before thread 0's device-scope fence and arrival.
+          // stores before thread 0's acquire-release arrival.
           named_bar_sync(1, cthreads);
           if (tid == 0) {
             const long long o_p = (long long)Hkv * pre[it.b] + (long long)it.j * it.nb;
             const int c_lo = cta_of(o_p, T, P);
             const int c_hi = cta_of(o_p + it.nb - 1, T, P);
-            __threadfence();
-            const int old = atomicAdd(&p.counters[pair], 1);
+            const int old = atomic_add_acq_rel_gpu(&p.counters[pair], 1);
             const bool last = old == c_hi - c_lo;
-            if (last) {
-              p.counters[pair] = 0;  // ready for the next call
-              __threadfence();
-            }
+            if (last) p.counters[pair] = 0;  // ready for the next call (ordered by the kernel boundary)
             *last_flag = last ? (c_lo + 1) : 0;  // encodes c_lo
             *chi_flag = c_hi;
           }

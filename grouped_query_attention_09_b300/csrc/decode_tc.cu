@@ -542,14 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long o_p = (long long)Hkv * pre[it.b] + (long long)it.j * it.nb;
             const int c_lo = owner_cta(o_p, T, P);
             const int c_hi = owner_cta(o_p + it.nb - 1, T, P);
-            __threadfence();
             const int pair = it.b * Hkv + it.j;
-            const int old = atomicAdd(&p.counters[pair], 1);
+            const int old = atomic_add_acq_rel_gpu(&p.counters[pair], 1);
             const bool lastc = old == c_hi - c_lo;
-            if (lastc) {
-              p.counters[pair] = 0;  // ready for the next call
-              __threadfence();
-            }
+            if (lastc) p.counters[pair] = 0;  // ready for the next call (ordered by the kernel boundary)
             *merge_flag = lastc ? c_lo + 1 : 0;
             *chi_flag = c_hi;
           } else if (r == 0) {

@@ -153,6 +153,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Device-scope atomic add with acquire-release semantics: the release
+// publishes every store ordered before it (including other threads' stores
+// ordered by a preceding barrier), the acquire makes other CTAs' published
+// stores visible to the loads that follow.  Returns the old value.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // True in exactly one lane of the (fully active) warp: elect.sync.
 __device__ __forceinline__ bool elect_one_sync() {
   uint32_t pred = 0;
