@@ -89,6 +89,43 @@ def make_decode_inputs(w: DecodeWorkload, tail: str = "randn", q_mult: float = 1
     return q, k, v, seqlens
 
 
+E4M3_MAX = 448.0
+E4M3_NAN = 0x7F
+
+
+def quantize_kv_fp8(k, v):
+    """FP8 E4M3 cache of bf16/fp32 K, V [B, Hkv, L, D]: one scale per (b, kv
+    head) for K and one for V, scale = max|x| / 448 over that head's rows, and
+    bytes = round-to-nearest-even E4M3 of x / scale (torch's float8_e4m3fn
+    conversion).  Returns (k8, v8) uint8 tensors and (k_scale, v_scale) fp32
+    [B, Hkv] tensors; the real cache entries are e4m3(byte) * scale."""
+    def one(x):
+        x = x.float()
+        amax = x.abs().amax(dim=(2, 3)).clamp(min=1e-30)
+        scale = amax / E4M3_MAX
+        q8 = (x / scale[:, :, None, None]).to(torch.float8_e4m3fn)
+        return q8.view(torch.uint8), scale.float()
+    k8, ks = one(k)
+    v8, vs = one(v)
+    return k8, v8, ks, vs
+
+
+def make_decode_fp8_inputs(w: DecodeWorkload, tail: str = "randn", q_mult: float = 1.0):
+    """q (bf16), k8, v8 (E4M3 bytes), k_scale, v_scale, seqlens of workload w:
+    the bf16 workload's draws (same seed and order), then quantize_kv_fp8.
+    tail="nan" writes the E4M3 NaN byte into cache rows t >= seqlens[b]."""
+    q, k, v, seqlens = make_decode_inputs(w, q_mult=q_mult)
+    k8, v8, ks, vs = quantize_kv_fp8(k, v)
+    if tail == "nan":
+        for b in range(k8.shape[0]):
+            n = max(int(seqlens[b]), 0)
+            k8[b, :, n:, :] = E4M3_NAN
+            v8[b, :, n:, :] = E4M3_NAN
+    elif tail != "randn":
+        raise ValueError(tail)
+    return q, k8, v8, ks, vs, seqlens
+
+
 def poison_tail(k, v, seqlens):
     """Fills cache rows t >= seqlens[b] with NaN (in place)."""
     for b in range(k.shape[0]):
@@ -125,6 +162,12 @@ def decode_kv_bytes(seqlens, Hkv: int, D: int, elem_bytes: int = 2) -> int:
     once per KV head (sum_b seqlens[b] * Hkv * D * 2 tensors * elem_bytes)."""
     total = int(torch.as_tensor(seqlens).clamp(min=0).sum())
     return kv_cache_bytes(1, total, Hkv * D, 1, elem_bytes)
+
+
+def decode_kv_bytes_fp8(seqlens, Hkv: int, D: int) -> int:
+    """Algorithmic bytes of a decode step over an FP8 cache: one byte per K/V
+    element of the visible rows (the per-head scales are negligible)."""
+    return decode_kv_bytes(seqlens, Hkv, D, elem_bytes=1)
 
 
 def decode_flops(seqlens, Hq: int, D: int) -> int:

@@ -56,6 +56,10 @@ def _load():
         lib.gqa_oracle_decode.restype = i
         lib.gqa_oracle_prefill.argtypes = [p, p, p, i, i, i, i, i, i, i, ctypes.c_double, p, i, p]
         lib.gqa_oracle_prefill.restype = i
+        lib.gqa_oracle_decode_fp8.argtypes = [p, i, p, p, p, p, p, i, i, i, i, i, ctypes.c_double, p, i, p]
+        lib.gqa_oracle_decode_fp8.restype = i
+        lib.gqa_oracle_e4m3_values.argtypes = [p, i, p]
+        lib.gqa_oracle_e4m3_values.restype = None
         lib.gqa_oracle_num_threads.restype = i
         _lib = lib
     return _lib
@@ -100,6 +104,40 @@ def decode(q, k_cache, v_cache, seqlens, scale=None, rows=None, check=True):
                                    B, Hq, Hkv, D, Lmax, float(scale), _ptr(r), n, _ptr(out))
     if check and rc not in (0,):
         raise ValueError(f"oracle decode returned {rc}")
+    return out.reshape(B, Hq, D) if r is None else out
+
+
+def e4m3_values(bytes_u8):
+    """Exact fp64 values of OCP FP8 E4M3 bytes (uint8 array)."""
+    b = np.ascontiguousarray(np.asarray(bytes_u8, dtype=np.uint8).reshape(-1))
+    out = np.empty(b.size, dtype=np.float64)
+    _load().gqa_oracle_e4m3_values(_ptr(b), b.size, _ptr(out))
+    return out.reshape(np.shape(bytes_u8))
+
+
+def decode_fp8(q, k8, v8, k_scale, v_scale, seqlens, scale=None, rows=None, check=True):
+    """Decode over an FP8 E4M3 cache: real K = e4m3(k8) * k_scale[b, j] (same
+    for V).  q [B, Hq, D] (bf16 bits or fp64); k8, v8 uint8 [B, Hkv, Lmax, D];
+    k_scale, v_scale [B, Hkv] (or [B * Hkv]).  Returns fp64 like decode()."""
+    (q,), etype = _prep(q)
+    k8 = np.ascontiguousarray(np.asarray(k8, dtype=np.uint8))
+    v8 = np.ascontiguousarray(np.asarray(v8, dtype=np.uint8))
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, D2 = k8.shape
+    if D2 != D or v8.shape != k8.shape or k8.shape[0] != B:
+        raise ValueError("shape mismatch")
+    ks = np.ascontiguousarray(np.asarray(k_scale, dtype=np.float64).reshape(B * Hkv))
+    vs = np.ascontiguousarray(np.asarray(v_scale, dtype=np.float64).reshape(B * Hkv))
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32).reshape(B))
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+    n = B * Hq if r is None else r.shape[0]
+    out = np.empty((n, D), dtype=np.float64)
+    rc = _load().gqa_oracle_decode_fp8(_ptr(q), etype, _ptr(k8), _ptr(v8), _ptr(ks), _ptr(vs), _ptr(sl),
+                                       B, Hq, Hkv, D, Lmax, float(scale), _ptr(r), n, _ptr(out))
+    if check and rc not in (0,):
+        raise ValueError(f"oracle decode_fp8 returned {rc}")
     return out.reshape(B, Hq, D) if r is None else out
 
 

@@ -32,6 +32,15 @@
  * one length L; row i sees keys t <= i when causal, all L keys otherwise.
  *
  * Element types: 0 = bf16 bit patterns (uint16), 1 = fp64.  Outputs are fp64.
+ *
+ * FP8 cache (gqa_oracle_decode_fp8): K and V are stored as OCP FP8 E4M3 bytes
+ * (sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 encodes
+ * subnormals m/8 * 2^-6; S.1111.111 is NaN; no infinities; largest 448) with
+ * one scale per (batch, KV head) for K and one for V: the real entry is the
+ * decoded byte times its scale ("InputsFp8" of the gsyq.cn page on xformers,
+ * "混合精度计算加速", names FP8 KV storage; the per-(sequence, KV head) scale
+ * is this build's reading).  Step (1) becomes: decode the byte exactly, then
+ * multiply by the scale in fp64.
  * Rows to evaluate are given as an index list so that sampled rows of a
  * full-size workload can be checked one by one.
  *
@@ -54,6 +63,19 @@ static double elem(const void *base, size_t i, int type)
     float f;
     memcpy(&f, &bits, sizeof f);
     return (double)f; /* step (1): exact */
+}
+
+/* Exact value of an OCP FP8 E4M3 byte. */
+static double e4m3_value(uint8_t byte)
+{
+    int sign = byte >> 7, e = (byte >> 3) & 15, m = byte & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        mag = ldexp((double)m, -9);          /* m/8 * 2^(1-7) */
+    else
+        mag = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+    return sign ? -mag : mag;
 }
 
 /* One query row against `nk` visible keys of one (b, h).
@@ -151,6 +173,68 @@ int gqa_oracle_decode(const void *q, const void *k, const void *v, int type,
         free(kx); free(vx); free(x); free(qrow);
     }
     return rc_all;
+}
+
+/* Decode over an FP8 E4M3 cache (see the header).
+ *   q        [B, Hq, D] of element type `type` (0 bf16 bits, 1 fp64)
+ *   k8, v8   [B, Hkv, Lmax, D] E4M3 bytes; k_scale, v_scale [B * Hkv] fp64
+ *   everything else as gqa_oracle_decode. */
+int gqa_oracle_decode_fp8(const void *q, int type, const uint8_t *k8, const uint8_t *v8,
+                          const double *k_scale, const double *v_scale, const int32_t *seqlens,
+                          int B, int Hq, int Hkv, int D, int Lmax, double scale,
+                          const int32_t *rows, int nrows, double *out)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax <= 0 || Hq % Hkv != 0) return 1;
+    if (type != 0 && type != 1) return 1;
+    if (rows == NULL) nrows = B * Hq;
+    for (int b = 0; b < B; ++b)
+        if (seqlens[b] > Lmax) return 1;
+    int n_rep = Hq / Hkv;
+    int rc_all = 0;
+#pragma omp parallel
+    {
+        double *kx = malloc(sizeof(double) * (size_t)Lmax * D);
+        double *vx = malloc(sizeof(double) * (size_t)Lmax * D);
+        double *x = malloc(sizeof(double) * (size_t)Lmax);
+        double *qrow = malloc(sizeof(double) * (size_t)D);
+        int oom = !(kx && vx && x && qrow);
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < nrows; ++r) {
+            int rc;
+            if (oom) {
+                rc = 2;
+            } else {
+                int b = rows ? rows[2 * r] : r / Hq;
+                int h = rows ? rows[2 * r + 1] : r % Hq;
+                if (b < 0 || b >= B || h < 0 || h >= Hq) {
+                    rc = 1;
+                } else {
+                    int n = seqlens[b] > 0 ? seqlens[b] : 0;
+                    int j = h / n_rep; /* step (2): the KV head of query head h */
+                    size_t base = (((size_t)b * Hkv + j) * Lmax) * D;
+                    double ks = k_scale[b * Hkv + j], vs = v_scale[b * Hkv + j];
+                    for (size_t i = 0; i < (size_t)n * D; ++i) {
+                        kx[i] = e4m3_value(k8[base + i]) * ks; /* step (1) for an FP8 cache */
+                        vx[i] = e4m3_value(v8[base + i]) * vs;
+                    }
+                    for (int d = 0; d < D; ++d) qrow[d] = elem(q, ((size_t)b * Hq + h) * D + d, type);
+                    rc = attend_row(qrow, kx, vx, n, D, scale, x, out + (size_t)r * D);
+                }
+            }
+            if (rc) {
+#pragma omp critical
+                if (rc_all == 0 || rc < rc_all) rc_all = rc;
+            }
+        }
+        free(kx); free(vx); free(x); free(qrow);
+    }
+    return rc_all;
+}
+
+/* Exact values of n E4M3 bytes (for tests of the decoding itself). */
+void gqa_oracle_e4m3_values(const uint8_t *bytes, int n, double *out)
+{
+    for (int i = 0; i < n; ++i) out[i] = e4m3_value(bytes[i]);
 }
 
 /* Prefill.

@@ -298,3 +298,69 @@ def test_sampled_rows_equal_full_evaluation(oracle_mod):
     partp = oracle_mod.prefill(W.bf16_bits(qp), W.bf16_bits(kp), W.bf16_bits(vp), rows=rows3)
     for r, (b, h, i) in enumerate(rows3):
         np.testing.assert_array_equal(partp[r], fullp[b, h, i])
+
+
+# ---- FP8 E4M3 cache (decode_fp8) --------------------------------------------
+
+def test_e4m3_decoding_matches_torch_on_all_bytes(oracle_mod):
+    """The oracle's E4M3 decoding against torch's float8_e4m3fn (a library
+    routine) on every byte value."""
+    b = np.arange(256, dtype=np.uint8)
+    mine = oracle_mod.e4m3_values(b)
+    ref = torch.from_numpy(b).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+
+
+def test_e4m3_closed_forms(oracle_mod):
+    """Format definition: bias 7, 3 mantissa bits, subnormals m/8 * 2^-6,
+    S.1111.111 NaN, largest 448."""
+    vals = oracle_mod.e4m3_values(np.array([0x38, 0xB8, 0x7E, 0x08, 0x01, 0x07, 0x00, 0x80, 0x3C], dtype=np.uint8))
+    assert list(vals) == [1.0, -1.0, 448.0, 2.0 ** -6, 2.0 ** -9, 7 * 2.0 ** -9, 0.0, -0.0, 1.5]
+    assert np.isnan(oracle_mod.e4m3_values(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+
+
+def _fp8_case(seed, B=3, Hq=8, Hkv=2, D=16, Lmax=40):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, Hq, D, generator=g, dtype=torch.float64)
+    k = torch.randn(B, Hkv, Lmax, D, generator=g)
+    v = torch.randn(B, Hkv, Lmax, D, generator=g)
+    k8 = (k * 40).clamp(-448, 448).to(torch.float8_e4m3fn)
+    v8 = (v * 40).clamp(-448, 448).to(torch.float8_e4m3fn)
+    ks = torch.rand(B, Hkv, generator=g, dtype=torch.float64) * 0.05 + 0.01
+    vs = torch.rand(B, Hkv, generator=g, dtype=torch.float64) * 0.05 + 0.01
+    sl = torch.tensor([Lmax, 1, 17][:B], dtype=torch.int32)
+    return q, k8, v8, ks, vs, sl
+
+
+def test_decode_fp8_equals_decode_of_dequantized_cache(oracle_mod):
+    """decode_fp8 = decode over the cache dequantised by torch (fp8 -> fp64,
+    times the per-(b, kv head) scale): the scales are applied per head."""
+    q, k8, v8, ks, vs, sl = _fp8_case(11)
+    kd = k8.double() * ks[:, :, None, None]
+    vd = v8.double() * vs[:, :, None, None]
+    a = oracle_mod.decode_fp8(q.numpy(), k8.view(torch.uint8).numpy(), v8.view(torch.uint8).numpy(),
+                              ks.numpy(), vs.numpy(), sl.numpy(), 0.3)
+    b = oracle_mod.decode(q.numpy(), kd.numpy(), vd.numpy(), sl.numpy(), 0.3)
+    assert np.array_equal(a, b)
+
+
+def test_decode_fp8_scale_identities(oracle_mod):
+    """Doubling a head's V scale doubles its output exactly; multiplying its K
+    scale by c is the same as multiplying the logit scale by c."""
+    q, k8, v8, ks, vs, sl = _fp8_case(12)
+    k8u, v8u = k8.view(torch.uint8).numpy(), v8.view(torch.uint8).numpy()
+    base = oracle_mod.decode_fp8(q.numpy(), k8u, v8u, ks.numpy(), vs.numpy(), sl.numpy(), 0.25)
+    dbl = oracle_mod.decode_fp8(q.numpy(), k8u, v8u, ks.numpy(), 2 * vs.numpy(), sl.numpy(), 0.25)
+    assert np.array_equal(dbl, 2 * base)
+    kc = oracle_mod.decode_fp8(q.numpy(), k8u, v8u, 4 * ks.numpy(), vs.numpy(), sl.numpy(), 0.25)
+    sc = oracle_mod.decode_fp8(q.numpy(), k8u, v8u, ks.numpy(), vs.numpy(), sl.numpy(), 1.0)
+    np.testing.assert_allclose(kc, sc, rtol=1e-12, atol=1e-12)
+    # group map: head h reads KV head h // G (group-constant V makes it visible)
+    v8c = np.zeros_like(v8u)
+    v8c[:, 0] = 0x38   # 1.0
+    v8c[:, 1] = 0x40   # 2.0
+    out = oracle_mod.decode_fp8(q.numpy(), k8u, v8c, ks.numpy(), np.ones((3, 2)), sl.numpy(), 0.25)
+    for h in range(8):
+        np.testing.assert_allclose(out[:, h, :], 1.0 + (h // 4), rtol=0, atol=1e-12)
