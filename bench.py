@@ -187,6 +187,22 @@ def bench_decode(g, W, name, dev, steps, warmup, flush, seed_offset=0):
             "flops": W.decode_flops(sl, w.Hq, w.D)}
 
 
+def bench_decode_fp8(g, W, name, dev, steps, warmup, flush):
+    """gqa_decode_fp8 on workload `name` with its cache quantised to E4M3."""
+    import torch
+    w = W.WORKLOADS[name]
+    q, k8, v8, ks, vs, sl = W.make_decode_fp8_inputs(w)
+    qd, kd, vd, ksd, vsd, sld = (t.to(dev) for t in (q, k8, v8, ks, vs, sl))
+    out = torch.empty_like(qd)
+    stream = torch.cuda.current_stream(dev)
+    ts = timed_launches(lambda: g.gqa_decode_fp8(qd, kd, vd, ksd, vsd, sld, out=out, scale=w.scale, stream=stream),
+                        steps, warmup, flush, stream)
+    flags = g.gqa_get_device_status()
+    if flags:
+        raise RuntimeError(f"decode fp8 {name}: device status {flags:#x}")
+    return {"w": w, "ms": ts, "bytes": W.decode_kv_bytes_fp8(sl, w.Hkv, w.D)}
+
+
 def bench_prefill(g, W, dev, steps, warmup, flush):
     import torch
     w = W.WORKLOADS["prefill"]
@@ -323,7 +339,10 @@ def run_only(g, W, args, dev, flush, peaks):
         tf = r["flops"] / (ms / 1e3) / 1e12
         print(json.dumps({"only": "prefill", "us": ms * 1e3, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]}))
         return 0
-    r = bench_decode(g, W, args.only, dev, args.steps, args.warmup, flush)
+    if args.only.endswith("_fp8"):
+        r = bench_decode_fp8(g, W, args.only[:-4], dev, args.steps, args.warmup, flush)
+    else:
+        r = bench_decode(g, W, args.only, dev, args.steps, args.warmup, flush)
     ms = statistics.mean(r["ms"])
     gbs = r["bytes"] / (ms / 1e3) / 1e9
     print(json.dumps({"only": args.only, "us": ms * 1e3, "us_min": min(r["ms"]) * 1e3, "GB/s": gbs,
@@ -387,6 +406,14 @@ def main():
         dw[HEADLINE] = {"us": mean_ms * 1e3, "kv_bytes": res["bytes"], "GB/s": achieved,
                         "frac_hbm": achieved / peaks["hbm_gbs"], "TFLOP/s": res["flops"] / (mean_ms / 1e3) / 1e12}
         extras["decode_workloads"] = dw
+        d8 = {}
+        for name in ("llama3_8b", "llama2_70b"):
+            r = bench_decode_fp8(g, W, name, dev, small_steps, args.warmup, flush)
+            ms = statistics.mean(r["ms"])
+            gbs = r["bytes"] / (ms / 1e3) / 1e9
+            d8[name] = {"us": ms * 1e3, "kv_bytes_fp8": r["bytes"], "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+                        "speedup_vs_bf16": dw[name]["us"] / (ms * 1e3)}
+        extras["decode_fp8_kv"] = d8
         pr = bench_prefill(g, W, dev, small_steps, args.warmup, flush)
         if pr is not None:
             pms = statistics.mean(pr["ms"])

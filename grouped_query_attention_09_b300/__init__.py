@@ -6,7 +6,7 @@ status.  All arithmetic runs in the library's CUDA kernels; there is no CPU
 or PyTorch fallback, and a missing or unloadable library raises.
 
 Names and semantics follow include/gqa.h:
-  gqa_decode, gqa_prefill, gqa_decode_host, gqa_prefill_host,
+  gqa_decode, gqa_decode_fp8, gqa_prefill, gqa_decode_host, gqa_prefill_host,
   gqa_status_string, gqa_get_device_status, gqa_decode_plan, gqa_release.
 """
 from __future__ import annotations
@@ -32,7 +32,7 @@ GQA_DEV_WAIT_TIMEOUT = 0x4
 
 EXPORTED = ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host",
             "gqa_status_string", "gqa_get_device_status", "gqa_decode_plan", "gqa_release",
-            "gqa_decode_noalloc")
+            "gqa_decode_noalloc", "gqa_decode_fp8")
 
 _lib = None
 
@@ -57,7 +57,9 @@ def load_library():
     lib.gqa_decode_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.gqa_prefill_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
-    for fn in ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host", "gqa_decode_noalloc"):
+    lib.gqa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    for fn in ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host", "gqa_decode_noalloc",
+               "gqa_decode_fp8"):
         getattr(lib, fn).restype = i
     lib.gqa_status_string.argtypes = [i]
     lib.gqa_status_string.restype = ctypes.c_char_p
@@ -133,6 +135,28 @@ def gqa_decode_noalloc(q, k_cache, v_cache, seqlens, out, scale=None, stream=Non
                                     _dev_ptr(seqlens, "seqlens", torch.int32), _dev_ptr(out, "out", torch.bfloat16),
                                     B, Hq, Hkv, D, Lmax, float(scale), _stream_ptr(stream, q.device))
     _check(st, "gqa_decode_noalloc")
+    return out
+
+
+def gqa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seqlens, out=None, scale=None, stream=None):
+    """Decode over an FP8 E4M3 cache.  q [B, Hq, D] bf16; k_cache/v_cache
+    [B, Hkv, Lmax, D] uint8 (E4M3 bytes); k_scale/v_scale [B, Hkv] fp32;
+    seqlens [B] int32 (device); returns out [B, Hq, D] bf16."""
+    import torch
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = D ** -0.5
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.gqa_decode_fp8(_dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k_cache, "k_cache", torch.uint8),
+                                _dev_ptr(v_cache, "v_cache", torch.uint8), _dev_ptr(k_scale, "k_scale", torch.float32),
+                                _dev_ptr(v_scale, "v_scale", torch.float32), _dev_ptr(seqlens, "seqlens", torch.int32),
+                                _dev_ptr(out, "out", torch.bfloat16), B, Hq, Hkv, D, Lmax, float(scale),
+                                _stream_ptr(stream, q.device))
+    _check(st, "gqa_decode_fp8")
     return out
 
 

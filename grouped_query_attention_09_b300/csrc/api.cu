@@ -108,9 +108,11 @@ int check_prefill_args(const void* q, const void* k, const void* v, const void* 
 }
 
 int decode_locked(DeviceCtx& c, const void* q, const void* k, const void* v, const int32_t* seqlens,
-                  void* out, int B, int Hq, int Hkv, int D, int Lmax, float scale, cudaStream_t s) {
+                  void* out, int B, int Hq, int Hkv, int D, int Lmax, float scale, cudaStream_t s,
+                  const float* k_scale = nullptr, const float* v_scale = nullptr) {
+  const bool kv8 = k_scale != nullptr;
   gqa::DecodePlan plan;
-  if (!gqa::decode_plan(B, Hq, Hkv, D, Lmax, c.sm_count, &plan)) return GQA_ERR_UNSUPPORTED;
+  if (!gqa::decode_plan(B, Hq, Hkv, D, Lmax, c.sm_count, &plan, 0, kv8)) return GQA_ERR_UNSUPPORTED;
   cudaError_t e;
   if (plan.ws_part_floats > c.ws_part_cap || plan.ws_counters > c.counters_cap) {
     // Growing the workspace: cudaFree waits for work that still uses the old one.
@@ -132,7 +134,7 @@ int decode_locked(DeviceCtx& c, const void* q, const void* k, const void* v, con
     }
   }
   if ((e = order_after_previous(c, s)) != cudaSuccess) return cuda_fail(e);
-  gqa::DecodeArgs a{q, k, v, seqlens, out, B, Hq, Hkv, D, Lmax, scale, c.ws_part, c.counters, c.err};
+  gqa::DecodeArgs a{q, k, v, seqlens, out, B, Hq, Hkv, D, Lmax, scale, c.ws_part, c.counters, c.err, k_scale, v_scale};
   if ((e = gqa::decode_launch(plan, a, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = mark_used(c, s)) != cudaSuccess) return cuda_fail(e);
   return GQA_OK;
@@ -179,6 +181,28 @@ CUresult encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t dim0, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+CUresult encode_tmap_u8_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                           uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t dims[3] = {dim0, dim1, dim2};
+  cuuint64_t strides[2] = {stride1, stride2};
+  cuuint32_t box[3] = {box0, box1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 }  // namespace gqa
 
 extern "C" {
@@ -192,6 +216,26 @@ int gqa_decode(const void* q, const void* k_cache, const void* v_cache, const in
   if ((st = get_ctx(&c)) != GQA_OK) return st;
   return decode_locked(*c, q, k_cache, v_cache, seqlens, out, B, Hq, Hkv, D, Lmax, scale,
                        static_cast<cudaStream_t>(stream));
+}
+
+int gqa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                   const float* v_scale, const int32_t* seqlens, void* out, int B, int Hq, int Hkv, int D,
+                   int Lmax, float scale, void* stream) {
+  if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !seqlens || !out) return GQA_ERR_NULL;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(seqlens) & 3u) || (reinterpret_cast<uintptr_t>(k_scale) & 3u) ||
+      (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return GQA_ERR_MISALIGNED;
+  gqa::DecodePlan plan;
+  if (!gqa::decode_plan(B, Hq, Hkv, D, Lmax, 148, &plan, 0, true)) return GQA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceCtx* c = nullptr;
+  int st = get_ctx(&c);
+  if (st != GQA_OK) return st;
+  return decode_locked(*c, q, k_cache, v_cache, seqlens, out, B, Hq, Hkv, D, Lmax, scale,
+                       static_cast<cudaStream_t>(stream), k_scale, v_scale);
 }
 
 int gqa_prefill(const void* q, const void* k, const void* v, void* out, int B, int L, int Hq, int Hkv,

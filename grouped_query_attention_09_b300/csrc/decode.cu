@@ -67,22 +67,26 @@ struct Params {
   int B, Hq, Hkv, G, Lmax;
   int HS, NC, stages, num_ctas;
   float scale_log2;
+  const float* k_scale;  // FP8 cache: per (b, kv head) scales of K and V
+  const float* v_scale;
 };
 
 struct SmemLayout {
   int stage_bytes, k_bytes;
-  int epi_off, red_off, q_off, pre_off, bar_off, flag_off, total;
+  int epi_off, red_off, q_off, pre_off, bar_off, flag_off, cvt_off, total;
 };
 
 __host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 // NG: groups of consumer warps that take alternate tiles (each group keeps
 // its own running state, merged at the end of a piece like the key slices).
+// kv8: the ring holds FP8 E4M3 tiles (one byte per element) and every tile
+// group has a private fp16 copy of its current V tile (cvt region).
 template <int D>
-__host__ __device__ inline SmemLayout smem_layout(int stages, int Gpad, int NG) {
+__host__ __device__ inline SmemLayout smem_layout(int stages, int Gpad, int NG, bool kv8 = false) {
   SmemLayout s;
   const int slices = kKW * NG;
-  s.k_bytes = (D / 64) * kBN * 128;
+  s.k_bytes = kv8 ? kBN * D : (D / 64) * kBN * 128;
   s.stage_bytes = 2 * s.k_bytes;
   s.epi_off = stages * s.stage_bytes;
   // epi holds the key-slice accumulators, later the merge statistics (2 x pieces x G)
@@ -91,7 +95,9 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int Gpad, int NG) 
   s.pre_off = round_up(s.q_off + Gpad * (D + 8) * 2, 16);
   s.bar_off = round_up(s.pre_off + (kMaxBatch + 1) * 4, 8);
   s.flag_off = s.bar_off + 2 * stages * 8;
-  s.total = s.flag_off + 4 * (4 + 32) + 1024;  // flags + scan scratch, + slack to align the base
+  s.cvt_off = round_up(s.flag_off + 4 * (4 + 32), 1024);
+  const int cvt_bytes = kv8 ? NG * (D / 64) * kBN * 128 : 0;  // one fp16 V tile per tile group
+  s.total = s.cvt_off + cvt_bytes + 1024;  // flags + scan scratch, fp16 copies, + slack to align the base
 
   return s;
 }
@@ -137,15 +143,16 @@ __device__ inline int clamp_len(int len, int Lmax) { return len < 0 ? 0 : (len >
 template <int NT>
 __host__ __device__ constexpr int tile_groups() { return NT == 1 ? 2 : 1; }
 
-template <int D, int NT>
+template <int D, int NT, bool KV8>
 __global__ void __launch_bounds__(288, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const Params p) {
   constexpr int KT = D / 16;  // 16-wide k-steps over D (QK) and m-tiles over D (PV)
   constexpr int NG = tile_groups<NT>();
   constexpr int KS = kKW * NG;  // key-slice states merged at the end of a piece
+  static_assert(!KV8 || (D == 128 && NT == 1), "the FP8 cache path is built for D = 128, G <= 8");
   const int Gpad = p.HS * 8 * NT;
-  const SmemLayout L = smem_layout<D>(p.stages, Gpad, NG);
+  const SmemLayout L = smem_layout<D>(p.stages, Gpad, NG, KV8);
   // Each tile group has a private ring of SG stages: tile i belongs to group
   // i % NG and takes stage (i % NG) * SG + (i / NG) % SG.  A group therefore
   // waits on use u of a stage only after it consumed use u - 1 itself, so a
@@ -254,10 +261,16 @@ __global__ void __launch_bounds__(288, 1)
         uint8_t* vdst = kdst + L.k_bytes;
         mbar_arrive_expect_tx(&full[s], L.stage_bytes);
         const int z = it.b * Hkv + it.j, y = it.lt * kBN;
+        if constexpr (KV8) {
+          // one 128-byte-wide box per tensor: a row of D = 128 E4M3 bytes
+          tma_load_3d(kdst, &tmK, 0, y, z, &full[s], pol);
+          tma_load_3d(vdst, &tmV, 0, y, z, &full[s], pol);
+        } else {
 #pragma unroll
-        for (int box = 0; box < D / 64; ++box) {
-          tma_load_3d(kdst + box * kBN * 128, &tmK, box * 64, y, z, &full[s], pol);
-          tma_load_3d(vdst + box * kBN * 128, &tmV, box * 64, y, z, &full[s], pol);
+          for (int box = 0; box < D / 64; ++box) {
+            tma_load_3d(kdst + box * kBN * 128, &tmK, box * 64, y, z, &full[s], pol);
+            tma_load_3d(vdst + box * kBN * 128, &tmV, box * 64, y, z, &full[s], pol);
+          }
         }
         issued = i + 1;
         iter_next(it, pre, B, Hkv);
@@ -310,6 +323,8 @@ __global__ void __launch_bounds__(288, 1)
     __nv_bfloat16* q_s = reinterpret_cast<__nv_bfloat16*>(smem + L.q_off);
     constexpr int kQRow = D + 8;  // padded row (elements): rows 16 B apart in the bank map
     int seg_lt0 = 0, len_b = 0;
+    float sl_pair = p.scale_log2;  // logit scale in log2 units (times the K scale of an FP8 cache)
+    float v_mul = 1.f;             // V scale of an FP8 cache
     bool live = true;
 
     TileIter it;
@@ -324,15 +339,29 @@ __global__ void __launch_bounds__(288, 1)
       if (seg_first) {
         seg_lt0 = it.lt;
         len_b = clamp_len(p.seqlens[it.b], p.Lmax);
+        if constexpr (KV8) {
+          sl_pair = p.scale_log2 * __ldg(p.k_scale + pair);
+          v_mul = __ldg(p.v_scale + pair);
+        }
         const __nv_bfloat16* qb = p.q + ((size_t)it.b * p.Hq + (size_t)it.j * G) * D;
         if constexpr (NT == 1) {
 #pragma unroll
           for (int kk = 0; kk < KT; ++kk) {
             const int hg = (lane >> 2);
             if (hg < G) {
-              const uint32_t* qp = reinterpret_cast<const uint32_t*>(qb + (size_t)hg * D + kk * 16 + 2 * (lane & 3));
-              qf[kk][0][0] = __ldg(qp);
-              qf[kk][0][1] = __ldg(qp + 4);
+              if constexpr (KV8) {
+                // fp16, in the permuted k order of the FP8 K fragments: in
+                // k-step kk, k = 2c, 2c+1, 2c+8, 2c+9 read
+                // d = 64 (kk / 4) + 16 c + 4 (kk % 4) + 0 .. 3
+                const uint2 qv = __ldg(reinterpret_cast<const uint2*>(qb + (size_t)hg * D + 64 * (kk >> 2) +
+                                                                     16 * (lane & 3) + 4 * (kk & 3)));
+                qf[kk][0][0] = bf16x2_to_f16x2(qv.x);
+                qf[kk][0][1] = bf16x2_to_f16x2(qv.y);
+              } else {
+                const uint32_t* qp = reinterpret_cast<const uint32_t*>(qb + (size_t)hg * D + kk * 16 + 2 * (lane & 3));
+                qf[kk][0][0] = __ldg(qp);
+                qf[kk][0][1] = __ldg(qp + 4);
+              }
             } else {
               qf[kk][0][0] = 0u;
               qf[kk][0][1] = 0u;
@@ -364,11 +393,36 @@ __global__ void __launch_bounds__(288, 1)
       const bool mine = (i % NG) == grp;
       if (live && mine) live = mbar_wait_bounded(&full[s], parity_of(i), abort_flag, p.err);
       if (live && mine) {
-        const uint32_t kbase = smem_u32(smem + s * L.stage_bytes);
-        const uint32_t vbase = kbase + L.k_bytes;
+        uint32_t kbase = smem_u32(smem + s * L.stage_bytes);
+        uint32_t vbase = kbase + L.k_bytes;
         const int valid = min(kBN, len_b - it.lt * kBN);  // >= 1
 
-        if (valid < key0 + 16) {
+        if constexpr (KV8) {
+          // This warp's 16 V rows, E4M3 -> fp16, into the group's fp16 tile
+          // (the layout of a bf16 tile: two 64-column halves, 128-byte rows,
+          // 16-byte chunk c of row r at chunk c ^ (r & 7)); rows at or past
+          // seqlens[b] become zeros.  Only this warp reads these rows.
+          constexpr int kTile16 = (D / 64) * kBN * 128;
+          uint8_t* vcv = smem + L.cvt_off + grp * kTile16;
+          const uint8_t* vsrc = smem + s * L.stage_bytes + L.k_bytes;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = lane + 32 * u;  // 16 rows x 8 chunks of 16 E4M3 bytes
+            const int row = key0 + (e >> 3), c = e & 7;
+            uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+            if (row < valid) {
+              const uint4 raw = *reinterpret_cast<const uint4*>(vsrc + row * 128 + ((c ^ (row & 7)) << 4));
+              lo = make_uint4(e4m3x2_to_f16x2(raw.x), e4m3x2_to_f16x2(raw.x >> 16), e4m3x2_to_f16x2(raw.y),
+                              e4m3x2_to_f16x2(raw.y >> 16));
+              hi = make_uint4(e4m3x2_to_f16x2(raw.z), e4m3x2_to_f16x2(raw.z >> 16), e4m3x2_to_f16x2(raw.w),
+                              e4m3x2_to_f16x2(raw.w >> 16));
+            }
+            uint8_t* dp = vcv + (c >> 2) * kBN * 128 + row * 128;
+            *reinterpret_cast<uint4*>(dp + ((((2 * c) & 7) ^ (row & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4*>(dp + ((((2 * c + 1) & 7) ^ (row & 7)) << 4)) = hi;
+          }
+          vbase = smem_u32(vcv);
+        } else if (valid < key0 + 16) {
           // Rows past the sequence end hold whatever the cache holds there
           // (possibly NaN); zero this warp's V rows so P = 0 stays 0.
           const int r0 = max(valid, key0);
@@ -390,13 +444,37 @@ __global__ void __launch_bounds__(288, 1)
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+        uint4 k8g = make_uint4(0, 0, 0, 0), k8h = make_uint4(0, 0, 0, 0);  // E4M3 K bytes, rows g and g + 8
 #pragma unroll
         for (int kk = 0; kk < KT; ++kk) {
           uint32_t a[4];
-          const int chunk = (kk & 3) * 2 + k_chunk_add;
-          ldmatrix_x4(a, kbase + (kk >> 2) * kBN * 128 + k_row * 128 + ((chunk ^ sw) << 4));
+          if constexpr (KV8) {
+            // E4M3 K rows g and g + 8 of this warp's 16 keys.  One 16-byte
+            // chunk per row serves four k-steps: in k-step kk the fragment's
+            // k = 2c, 2c+1 | 2c+8, 2c+9 read bytes 4 (kk % 4) .. +3 of chunk
+            // 4 (kk / 4) + c (the q fragments use the same permutation).
+            const int g = key0 + (lane >> 2);
+            if ((kk & 3) == 0) {
+              const uint8_t* kt = smem + s * L.stage_bytes;
+              const int ch = 4 * (kk >> 2) + (lane & 3);
+              k8g = *reinterpret_cast<const uint4*>(kt + g * 128 + ((ch ^ (g & 7)) << 4));
+              k8h = *reinterpret_cast<const uint4*>(kt + (g + 8) * 128 + ((ch ^ (g & 7)) << 4));
+            }
+            const uint32_t w0 = (kk & 3) == 0 ? k8g.x : (kk & 3) == 1 ? k8g.y : (kk & 3) == 2 ? k8g.z : k8g.w;
+            const uint32_t w1 = (kk & 3) == 0 ? k8h.x : (kk & 3) == 1 ? k8h.y : (kk & 3) == 2 ? k8h.z : k8h.w;
+            a[0] = e4m3x2_to_f16x2(w0);
+            a[1] = e4m3x2_to_f16x2(w1);
+            a[2] = e4m3x2_to_f16x2(w0 >> 16);
+            a[3] = e4m3x2_to_f16x2(w1 >> 16);
+          } else {
+            const int chunk = (kk & 3) * 2 + k_chunk_add;
+            ldmatrix_x4(a, kbase + (kk >> 2) * kBN * 128 + k_row * 128 + ((chunk ^ sw) << 4));
+          }
           if constexpr (NT == 1) {
-            mma_bf16_16816(sc[0], a, qf[kk][0][0], qf[kk][0][1]);
+            if constexpr (KV8)
+              mma_f16_16816(sc[0], a, qf[kk][0][0], qf[kk][0][1]);
+            else
+              mma_bf16_16816(sc[0], a, qf[kk][0][0], qf[kk][0][1]);
           } else {
             // B fragments of both n-tiles for this k-step: matrices
             // (nt, d-lo), (nt, d-hi) for nt = 0, 1; lane l addresses head
@@ -410,6 +488,12 @@ __global__ void __launch_bounds__(288, 1)
           }
         }
 
+        if constexpr (KV8) {
+          // This warp has read its K and V rows of the E4M3 stage.
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+        }
+
         // ---- online softmax (log2 domain); rows = keys, columns = heads
         const bool v_lo = key0 + (lane >> 2) < valid;
         const bool v_hi = key0 + (lane >> 2) + 8 < valid;
@@ -417,10 +501,10 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           float x[4];
-          x[0] = v_lo ? sc[nt][0] * p.scale_log2 : -INFINITY;
-          x[1] = v_lo ? sc[nt][1] * p.scale_log2 : -INFINITY;
-          x[2] = v_hi ? sc[nt][2] * p.scale_log2 : -INFINITY;
-          x[3] = v_hi ? sc[nt][3] * p.scale_log2 : -INFINITY;
+          x[0] = v_lo ? sc[nt][0] * sl_pair : -INFINITY;
+          x[1] = v_lo ? sc[nt][1] * sl_pair : -INFINITY;
+          x[2] = v_hi ? sc[nt][2] * sl_pair : -INFINITY;
+          x[3] = v_hi ? sc[nt][3] * sl_pair : -INFINITY;
           float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
           for (int o = 4; o < 32; o <<= 1) {
@@ -443,8 +527,13 @@ __global__ void __launch_bounds__(288, 1)
             acc[kk][nt][2] *= al0;
             acc[kk][nt][3] *= al1;
           }
-          pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
-          pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+          if constexpr (KV8) {
+            pb[nt][0] = movmatrix_trans(pack_f16x2(p0, p1));
+            pb[nt][1] = movmatrix_trans(pack_f16x2(p2, p3));
+          } else {
+            pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
+            pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+          }
         }
 
         // ---- O^T += V^T P^T
@@ -454,10 +543,15 @@ __global__ void __launch_bounds__(288, 1)
           const int chunk = (mt & 3) * 2 + v_chunk_add;
           ldmatrix_x4_trans(a, vbase + (mt >> 2) * kBN * 128 + v_row * 128 + ((chunk ^ sw) << 4));
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a, pb[nt][0], pb[nt][1]);
+          for (int nt = 0; nt < NT; ++nt) {
+            if constexpr (KV8)
+              mma_f16_16816(acc[mt][nt], a, pb[nt][0], pb[nt][1]);
+            else
+              mma_bf16_16816(acc[mt][nt], a, pb[nt][0], pb[nt][1]);
+          }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (!KV8 && lane == 0) mbar_arrive(&empty[s]);
       }
 
       if (seg_last) {
@@ -482,10 +576,11 @@ __global__ void __launch_bounds__(288, 1)
             const int hg = (hs * NT + nt) * 8 + 2 * (lane & 3);
             float* e0 = epi + (size_t)(slice * Gpad + hg) * (D + 4);
             float* e1 = e0 + (D + 4);
-            e0[d] = acc[mt][nt][0];
-            e1[d] = acc[mt][nt][1];
-            e0[d + 8] = acc[mt][nt][2];
-            e1[d + 8] = acc[mt][nt][3];
+            // (an FP8 cache's V scale is applied here, once per piece)
+            e0[d] = KV8 ? acc[mt][nt][0] * v_mul : acc[mt][nt][0];
+            e1[d] = KV8 ? acc[mt][nt][1] * v_mul : acc[mt][nt][1];
+            e0[d + 8] = KV8 ? acc[mt][nt][2] * v_mul : acc[mt][nt][2];
+            e1[d + 8] = KV8 ? acc[mt][nt][3] * v_mul : acc[mt][nt][3];
           }
         }
         // The running state now lives in shared memory; resetting it here
@@ -652,7 +747,7 @@ __global__ void __launch_bounds__(288, 1)
 struct TmapEntry {
   const void* k;
   const void* v;
-  int D, Lmax;
+  int D, Lmax, kv8;
   uint64_t pairs;
   CUtensorMap tk, tv;
 };
@@ -661,27 +756,37 @@ std::mutex g_tmap_mu;
 TmapEntry g_tmap_cache[kTmapCacheSize];
 int g_tmap_n = 0, g_tmap_next = 0;
 
-cudaError_t cache_tensor_maps(const DecodeArgs& a, int D, CUtensorMap* tk, CUtensorMap* tv) {
+cudaError_t cache_tensor_maps(const DecodeArgs& a, int D, bool kv8, CUtensorMap* tk, CUtensorMap* tv) {
   const uint64_t pairs = (uint64_t)a.B * a.Hkv;
   std::lock_guard<std::mutex> lk(g_tmap_mu);
   for (int e = 0; e < g_tmap_n; ++e) {
     const TmapEntry& c = g_tmap_cache[e];
-    if (c.k == a.k_cache && c.v == a.v_cache && c.D == D && c.Lmax == a.Lmax && c.pairs == pairs) {
+    if (c.k == a.k_cache && c.v == a.v_cache && c.D == D && c.Lmax == a.Lmax && c.pairs == pairs &&
+        c.kv8 == (int)kv8) {
       *tk = c.tk;
       *tv = c.tv;
       return cudaSuccess;
     }
   }
-  const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)a.Lmax * D * 2;
   TmapEntry n;
   n.k = a.k_cache;
   n.v = a.v_cache;
   n.D = D;
   n.Lmax = a.Lmax;
+  n.kv8 = (int)kv8;
   n.pairs = pairs;
-  if (encode_tmap_bf16_3d(&n.tk, a.k_cache, D, a.Lmax, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS ||
-      encode_tmap_bf16_3d(&n.tv, a.v_cache, D, a.Lmax, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  if (kv8) {
+    // E4M3 bytes: one 128-byte box covers a row of D = 128 elements
+    const uint64_t s1 = (uint64_t)D, s2 = (uint64_t)a.Lmax * D;
+    if (encode_tmap_u8_3d(&n.tk, a.k_cache, D, a.Lmax, pairs, s1, s2, D, kBN, 1) != CUDA_SUCCESS ||
+        encode_tmap_u8_3d(&n.tv, a.v_cache, D, a.Lmax, pairs, s1, s2, D, kBN, 1) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  } else {
+    const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)a.Lmax * D * 2;
+    if (encode_tmap_bf16_3d(&n.tk, a.k_cache, D, a.Lmax, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS ||
+        encode_tmap_bf16_3d(&n.tv, a.v_cache, D, a.Lmax, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   g_tmap_cache[g_tmap_next] = n;
   g_tmap_next = (g_tmap_next + 1) % kTmapCacheSize;
   if (g_tmap_n < kTmapCacheSize) ++g_tmap_n;
@@ -690,10 +795,10 @@ cudaError_t cache_tensor_maps(const DecodeArgs& a, int D, CUtensorMap* tk, CUten
   return cudaSuccess;
 }
 
-template <int D, int NT>
+template <int D, int NT, bool KV8>
 cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream) {
   CUtensorMap tmK, tmV;
-  cudaError_t e = cache_tensor_maps(a, D, &tmK, &tmV);
+  cudaError_t e = cache_tensor_maps(a, D, KV8, &tmK, &tmV);
   if (e != cudaSuccess) return e;
   Params p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
@@ -713,7 +818,9 @@ cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t s
   p.stages = plan.stages;
   p.num_ctas = plan.num_ctas;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  auto kern = decode_kernel<D, NT>;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  auto kern = decode_kernel<D, NT, KV8>;
   // The opt-in shared-memory size is a per-device function attribute: set it
   // once per device to the largest size any plan can ask for.
   static std::atomic<unsigned long long> attr_set{0};  // bit d: set on device d (< 64)
@@ -730,18 +837,22 @@ cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t s
 
 }  // namespace
 
-bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan, size_t max_part_floats) {
+bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan, size_t max_part_floats,
+                 bool kv8) {
   if (B < 1 || B > kMaxBatch || Hkv < 1 || Hq % Hkv != 0 || Lmax < 1) return false;
   if (D != 64 && D != 128) return false;
   const int G = Hq / Hkv;
+  // An FP8 cache runs on the warp-level kernel, built for D = 128, G <= 8.
+  if (kv8 && (D != 128 || G > 8)) return false;
   // Wide groups at D = 128 go to the tcgen05 kernel: its tensor core reads
   // each K/V block from shared memory once for all G heads.
-  if (D == 128 && G > 8 && G <= 128) {
+  if (!kv8 && D == 128 && G > 8 && G <= 128) {
     if (!decode_tc_plan(B, Hq, Hkv, D, Lmax, sm_count, plan)) return false;
     if (max_part_floats > 0 && plan->ws_part_floats > max_part_floats) return false;
     return true;
   }
   plan->kind = 0;
+  plan->kv8 = kv8;
   int Gpad, NT, HS;
   if (G <= 8) {
     Gpad = 8; NT = 1; HS = 1;
@@ -769,12 +880,12 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
     const long long pairs = (long long)B * Hkv;
     if (pairs <= plan->num_ctas && pairs * 4 >= (long long)plan->num_ctas * 3) plan->num_ctas = (int)pairs;
   }
-  SmemLayout l0 = D == 64 ? smem_layout<64>(0, Gpad, NG) : smem_layout<128>(0, Gpad, NG);
+  SmemLayout l0 = D == 64 ? smem_layout<64>(0, Gpad, NG, kv8) : smem_layout<128>(0, Gpad, NG, kv8);
   int stages = std::min(kMaxStages, (kSmemLimit - l0.total - 2 * kMaxStages * 8) / l0.stage_bytes);
   stages = stages / NG * NG;  // every tile group gets a private ring of stages / NG
   if (stages / NG < 2) return false;
   plan->stages = stages;
-  plan->smem_bytes = (size_t)(D == 64 ? smem_layout<64>(stages, Gpad, NG) : smem_layout<128>(stages, Gpad, NG)).total;
+  plan->smem_bytes = (size_t)(D == 64 ? smem_layout<64>(stages, Gpad, NG, kv8) : smem_layout<128>(stages, Gpad, NG, kv8)).total;
   plan->ws_part_floats = (size_t)plan->num_ctas * 2 * G * (D + 2);
   if (max_part_floats > 0 && plan->ws_part_floats > max_part_floats) return false;
   plan->chunk_tiles = 0;  // static split: one contiguous share per CTA
@@ -785,10 +896,14 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
 
 cudaError_t decode_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream) {
   if (plan.kind == 1) return decode_tc_launch(plan, a, stream);
-  if (plan.D == 128) {
-    return plan.NT == 1 ? launch_t<128, 1>(plan, a, stream) : launch_t<128, 2>(plan, a, stream);
+  if (plan.kv8) {
+    if (plan.D != 128 || plan.NT != 1 || !a.k_scale || !a.v_scale) return cudaErrorInvalidValue;
+    return launch_t<128, 1, true>(plan, a, stream);
   }
-  return plan.NT == 1 ? launch_t<64, 1>(plan, a, stream) : launch_t<64, 2>(plan, a, stream);
+  if (plan.D == 128) {
+    return plan.NT == 1 ? launch_t<128, 1, false>(plan, a, stream) : launch_t<128, 2, false>(plan, a, stream);
+  }
+  return plan.NT == 1 ? launch_t<64, 1, false>(plan, a, stream) : launch_t<64, 2, false>(plan, a, stream);
 }
 
 }  // namespace gqa

@@ -12,10 +12,14 @@ namespace gqa {
 CUresult encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1,
                              uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
                              uint32_t box1, uint32_t box2);
+// The same for a byte tensor (FP8 cache stored as uint8).
+CUresult encode_tmap_u8_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                           uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2);
 
 // ------------------------------------------------------------------ decode
 struct DecodePlan {
   int kind;                // 0: warp-level MMA kernel (decode.cu), 1: tcgen05 kernel (decode_tc.cu)
+  bool kv8;                // FP8 E4M3 cache (warp-level kernel, D = 128, G <= 8)
   int D, G, Gpad, NT, HS;  // head dim, group size, padded group, n-tiles/warp, head slices
   int tile_keys;           // keys per pipeline tile
   int chunk_tiles;         // tiles per scheduling chunk (unit of work a CTA claims)
@@ -33,7 +37,7 @@ struct DecodePlan {
 // max_part_floats bounds the partial-result workspace: the chunks grow
 // coarser until it fits.
 bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan,
-                 size_t max_part_floats = 0);
+                 size_t max_part_floats = 0, bool kv8 = false);
 
 struct DecodeArgs {
   const void* q;
@@ -46,6 +50,8 @@ struct DecodeArgs {
   float* ws_part;     // >= plan.ws_part_floats floats
   int* ws_counters;   // >= plan.ws_counters ints, zero on entry, zero on exit
   unsigned* err;      // device status word
+  const float* k_scale = nullptr;  // FP8 cache: [B * Hkv] scales of K and V
+  const float* v_scale = nullptr;
 };
 
 cudaError_t decode_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream);

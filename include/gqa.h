@@ -99,6 +99,31 @@ GQA_API int gqa_decode(const void* q, const void* k_cache, const void* v_cache, 
                void* out, int B, int Hq, int Hkv, int D, int Lmax, float scale, void* stream);
 
 /*
+ * gqa_decode_fp8 -- gqa_decode over a KV cache stored in 8 bits: OCP FP8 E4M3
+ * bytes (sign, 4 exponent bits with bias 7, 3 mantissa bits; largest 448)
+ * with one fp32 scale per (sequence, KV head) for K and one for V, so the
+ * real entry is e4m3(byte) * scale ("InputsFp8", FP8 KV storage, on the
+ * gsyq.cn page on xformers, "混合精度计算加速"; the scale granularity is this
+ * library's choice).  It halves the bytes the bandwidth-bound decode reads.
+ *
+ *   k_cache, v_cache  [B, Hkv, Lmax, D]  uint8 (E4M3 bytes), device
+ *   k_scale, v_scale  [B, Hkv]            fp32, device (4-byte aligned)
+ *   everything else as gqa_decode.
+ *
+ * Arithmetic: the E4M3 values are converted exactly to fp16 in shared memory;
+ * q is rounded to fp16 (so |q| must stay below 65504), scores and softmax are
+ * fp32, P is rounded to fp16, accumulation is fp32; the K scale multiplies
+ * the logit scale and the V scale the output.  Cache rows at or beyond
+ * seqlens[b] are never used (they may hold anything, NaN bytes included).
+ *
+ * Supported: D == 128, G = Hq/Hkv <= 8, 1 <= B <= 1024.  Otherwise
+ * GQA_ERR_UNSUPPORTED.  Workspace, streams and device status as gqa_decode.
+ */
+GQA_API int gqa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                           const float* v_scale, const int32_t* seqlens, void* out, int B, int Hq, int Hkv,
+                           int D, int Lmax, float scale, void* stream);
+
+/*
  * gqa_prefill -- attention of L query tokens over the same L keys (prompt
  * processing), causal or not.
  *
