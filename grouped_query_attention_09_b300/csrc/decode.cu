@@ -83,14 +83,16 @@ __host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m *
 // kv8: the ring holds FP8 E4M3 tiles (one byte per element) and every tile
 // group has a private fp16 copy of its current V tile (cvt region).
 template <int D>
-__host__ __device__ inline SmemLayout smem_layout(int stages, int Gpad, int NG, bool kv8 = false) {
+__host__ __device__ inline SmemLayout smem_layout(int stages, int Gpad, int NG, bool kv8, int G) {
   SmemLayout s;
   const int slices = kKW * NG;
   s.k_bytes = kv8 ? kBN * D : (D / 64) * kBN * 128;
   s.stage_bytes = 2 * s.k_bytes;
   s.epi_off = stages * s.stage_bytes;
   // epi holds the key-slice accumulators, later the merge statistics (2 x pieces x G)
-  s.red_off = s.epi_off + (slices * (D + 4) > 2 * kMaxCtas ? slices * (D + 4) : 2 * kMaxCtas) * Gpad * 4;
+  // epi: one row of D + 4 floats per (key slice, real head) -- sized by G, not
+  // the padded head count, which leaves room for one more ring stage at G = 4
+  s.red_off = s.epi_off + (slices * (D + 4) > 2 * kMaxCtas ? slices * (D + 4) : 2 * kMaxCtas) * G * 4;
   s.q_off = s.red_off + 2 * slices * Gpad * 4;  // [Gpad][D + 8] bf16 (NT = 2 only)
   s.pre_off = round_up(s.q_off + Gpad * (D + 8) * 2, 16);
   s.bar_off = round_up(s.pre_off + (kMaxBatch + 1) * 4, 8);
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(288, 1)
   constexpr int KS = kKW * NG;  // key-slice states merged at the end of a piece
   static_assert(!KV8 || (D == 128 && NT == 1), "the FP8 cache path is built for D = 128, G <= 8");
   const int Gpad = p.HS * 8 * NT;
-  const SmemLayout L = smem_layout<D>(p.stages, Gpad, NG, KV8);
+  const SmemLayout L = smem_layout<D>(p.stages, Gpad, NG, KV8, p.G);
   // Each tile group has a private ring of SG stages: tile i belongs to group
   // i % NG and takes stage (i % NG) * SG + (i / NG) % SG.  A group therefore
   // waits on use u of a stage only after it consumed use u - 1 itself, so a
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(288, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* epi = reinterpret_cast<float*>(smem + L.epi_off);          // [KW][Gpad][D+4]
+  float* epi = reinterpret_cast<float*>(smem + L.epi_off);          // [KS][G][D+4]
   float* red_m = reinterpret_cast<float*>(smem + L.red_off);        // [KW][Gpad]
   float* red_l = red_m + KS * Gpad;                                  // [KS][Gpad]
   int* pre = reinterpret_cast<int*>(smem + L.pre_off);               // [B+1]
@@ -574,13 +576,17 @@ __global__ void __launch_bounds__(288, 1)
           for (int mt = 0; mt < KT; ++mt) {
             const int d = mt * 16 + (lane >> 2);
             const int hg = (hs * NT + nt) * 8 + 2 * (lane & 3);
-            float* e0 = epi + (size_t)(slice * Gpad + hg) * (D + 4);
+            float* e0 = epi + (size_t)(slice * G + hg) * (D + 4);  // rows of padding heads are not kept
             float* e1 = e0 + (D + 4);
             // (an FP8 cache's V scale is applied here, once per piece)
-            e0[d] = KV8 ? acc[mt][nt][0] * v_mul : acc[mt][nt][0];
-            e1[d] = KV8 ? acc[mt][nt][1] * v_mul : acc[mt][nt][1];
-            e0[d + 8] = KV8 ? acc[mt][nt][2] * v_mul : acc[mt][nt][2];
-            e1[d + 8] = KV8 ? acc[mt][nt][3] * v_mul : acc[mt][nt][3];
+            if (hg < G) {
+              e0[d] = KV8 ? acc[mt][nt][0] * v_mul : acc[mt][nt][0];
+              e0[d + 8] = KV8 ? acc[mt][nt][2] * v_mul : acc[mt][nt][2];
+            }
+            if (hg + 1 < G) {
+              e1[d] = KV8 ? acc[mt][nt][1] * v_mul : acc[mt][nt][1];
+              e1[d + 8] = KV8 ? acc[mt][nt][3] * v_mul : acc[mt][nt][3];
+            }
           }
         }
         // The running state now lives in shared memory; resetting it here
@@ -629,7 +635,7 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
           for (int k = 0; k < KS; ++k) {
             const float f = red_m[k * Gpad + h];
-            const float4 x = *reinterpret_cast<const float4*>(epi + (size_t)(k * Gpad + h) * (D + 4) + d);
+            const float4 x = *reinterpret_cast<const float4*>(epi + (size_t)(k * G + h) * (D + 4) + d);
             acc4.x += f * x.x;
             acc4.y += f * x.y;
             acc4.z += f * x.z;
@@ -880,12 +886,12 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
     const long long pairs = (long long)B * Hkv;
     if (pairs <= plan->num_ctas && pairs * 4 >= (long long)plan->num_ctas * 3) plan->num_ctas = (int)pairs;
   }
-  SmemLayout l0 = D == 64 ? smem_layout<64>(0, Gpad, NG, kv8) : smem_layout<128>(0, Gpad, NG, kv8);
+  SmemLayout l0 = D == 64 ? smem_layout<64>(0, Gpad, NG, kv8, G) : smem_layout<128>(0, Gpad, NG, kv8, G);
   int stages = std::min(kMaxStages, (kSmemLimit - l0.total - 2 * kMaxStages * 8) / l0.stage_bytes);
   stages = stages / NG * NG;  // every tile group gets a private ring of stages / NG
   if (stages / NG < 2) return false;
   plan->stages = stages;
-  plan->smem_bytes = (size_t)(D == 64 ? smem_layout<64>(stages, Gpad, NG, kv8) : smem_layout<128>(stages, Gpad, NG, kv8)).total;
+  plan->smem_bytes = (size_t)(D == 64 ? smem_layout<64>(stages, Gpad, NG, kv8, G) : smem_layout<128>(stages, Gpad, NG, kv8, G)).total;
   plan->ws_part_floats = (size_t)plan->num_ctas * 2 * G * (D + 2);
   if (max_part_floats > 0 && plan->ws_part_floats > max_part_floats) return false;
   plan->chunk_tiles = 0;  // static split: one contiguous share per CTA
