@@ -60,6 +60,8 @@ def _load():
         lib.gqa_oracle_decode_fp8.restype = i
         lib.gqa_oracle_e4m3_values.argtypes = [p, i, p]
         lib.gqa_oracle_e4m3_values.restype = None
+        lib.gqa_oracle_rope_append.argtypes = [p, p, p, i, p, i, i, i, i, i, ctypes.c_double, p, p, p]
+        lib.gqa_oracle_rope_append.restype = i
         lib.gqa_oracle_num_threads.restype = i
         _lib = lib
     return _lib
@@ -139,6 +141,28 @@ def decode_fp8(q, k8, v8, k_scale, v_scale, seqlens, scale=None, rows=None, chec
     if check and rc not in (0,):
         raise ValueError(f"oracle decode_fp8 returned {rc}")
     return out.reshape(B, Hq, D) if r is None else out
+
+
+def rope_append(q, k_new, v_new, seqlens, Lmax, base=10000.0, check=True):
+    """The new token of sequence b at position p = seqlens[b]: rotary embedding
+    of its query and key heads at p (Llama rotate-half form, angle
+    p * base^(-2i/D) for the pair (i, i + D/2)).  q [B, Hq, D]; k_new, v_new
+    [B, Hkv, D] (bf16 bits or fp64).  Returns fp64 (q_out, k_row, v_row):
+    the rotated query, and the key / value rows that become cache row p."""
+    (q, k_new, v_new), etype = _prep(q, k_new, v_new)
+    B, Hq, D = q.shape
+    _, Hkv, D2 = k_new.shape
+    if D2 != D or v_new.shape != k_new.shape or k_new.shape[0] != B:
+        raise ValueError("shape mismatch")
+    sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32).reshape(B))
+    q_out = np.empty((B, Hq, D), dtype=np.float64)
+    k_row = np.empty((B, Hkv, D), dtype=np.float64)
+    v_row = np.empty((B, Hkv, D), dtype=np.float64)
+    rc = _load().gqa_oracle_rope_append(_ptr(q), _ptr(k_new), _ptr(v_new), etype, _ptr(sl), B, Hq, Hkv, D,
+                                        int(Lmax), float(base), _ptr(q_out), _ptr(k_row), _ptr(v_row))
+    if check and rc != 0:
+        raise ValueError(f"oracle rope_append returned {rc}")
+    return q_out, k_row, v_row
 
 
 def prefill(q, k, v, causal=True, scale=None, rows=None, check=True):

@@ -293,6 +293,60 @@ int gqa_oracle_prefill(const void *q, const void *k, const void *v, int type,
     return rc_all;
 }
 
+/* Rotary position embedding of one head vector x[D] at position pos, in place
+ * (the `apply_rotary_pos_emb(query_states, key_states, cos, sin)` of the GQA
+ * paper notes, "QA 相关"; the pages do not spell the rotation out, and this
+ * is the plainest reading of it, the Llama "rotate half" form): for
+ * i < D/2, the pair (x[i], x[i + D/2]) is rotated by the angle
+ * pos * base^(-2i/D). */
+static void rope_row(double *x, int D, double pos, double base)
+{
+    int half = D / 2;
+    for (int i = 0; i < half; ++i) {
+        double theta = pos * pow(base, -2.0 * i / D);
+        double c = cos(theta), s = sin(theta);
+        double x1 = x[i], x2 = x[i + half];
+        x[i] = x1 * c - x2 * s;
+        x[i + half] = x2 * c + x1 * s;
+    }
+}
+
+/* The step before a decode: the new token of every sequence b sits at
+ * position p = seqlens[b]; its query heads and its key heads are rotated at
+ * p, and its key and value heads become row p of the cache (the Huawei Cloud
+ * post, sections 2 and 5: the new K, V are concatenated to the layer's cache
+ * along the sequence).
+ *   q [B, Hq, D], k_new, v_new [B, Hkv, D] (element type `type`)
+ *   q_out [B, Hq, D], k_row, v_row [B, Hkv, D]: fp64 results (v_row = v_new)
+ * Returns 0, or 4 if some seqlens[b] >= Lmax (that row is not defined). */
+int gqa_oracle_rope_append(const void *q, const void *k_new, const void *v_new, int type,
+                           const int32_t *seqlens, int B, int Hq, int Hkv, int D, int Lmax,
+                           double base, double *q_out, double *k_row, double *v_row)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || D % 2 || Lmax <= 0 || Hq % Hkv != 0) return 1;
+    if (type != 0 && type != 1) return 1;
+    int rc = 0;
+    for (int b = 0; b < B; ++b) {
+        int p = seqlens[b] < 0 ? 0 : seqlens[b];
+        if (p >= Lmax) rc = 4;
+        for (int h = 0; h < Hq; ++h) {
+            double *x = q_out + ((size_t)b * Hq + h) * D;
+            for (int d = 0; d < D; ++d) x[d] = elem(q, ((size_t)b * Hq + h) * D + d, type);
+            rope_row(x, D, (double)p, base);
+        }
+        for (int j = 0; j < Hkv; ++j) {
+            double *x = k_row + ((size_t)b * Hkv + j) * D;
+            double *y = v_row + ((size_t)b * Hkv + j) * D;
+            for (int d = 0; d < D; ++d) {
+                x[d] = elem(k_new, ((size_t)b * Hkv + j) * D + d, type);
+                y[d] = elem(v_new, ((size_t)b * Hkv + j) * D + d, type);
+            }
+            rope_row(x, D, (double)p, base);
+        }
+    }
+    return rc;
+}
+
 int gqa_oracle_num_threads(void)
 {
 #ifdef _OPENMP

@@ -364,3 +364,67 @@ def test_decode_fp8_scale_identities(oracle_mod):
     out = oracle_mod.decode_fp8(q.numpy(), k8u, v8c, ks.numpy(), np.ones((3, 2)), sl.numpy(), 0.25)
     for h in range(8):
         np.testing.assert_allclose(out[:, h, :], 1.0 + (h // 4), rtol=0, atol=1e-12)
+
+
+# ---- rotary embedding of the new token + cache append (rope_append) ---------
+
+def _rope(oracle_mod, x, pos, base=10000.0):
+    """Rotate rows x [n, D] (fp64) at integer positions pos [n] with the oracle."""
+    n, D = x.shape
+    qo, _, _ = oracle_mod.rope_append(x.reshape(n, 1, D), np.zeros((n, 1, D)), np.zeros((n, 1, D)),
+                                      np.asarray(pos, dtype=np.int32), Lmax=1 << 30, base=base)
+    return qo.reshape(n, D)
+
+
+def test_rope_position_zero_is_identity(oracle_mod):
+    x = np.random.default_rng(1).standard_normal((5, 64))
+    assert np.array_equal(_rope(oracle_mod, x, [0] * 5), x)
+
+
+def test_rope_preserves_pair_norms(oracle_mod):
+    """Each (x_i, x_{i+D/2}) pair is rotated, so its length is unchanged."""
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((7, 128))
+    y = _rope(oracle_mod, x, rng.integers(0, 20000, 7))
+    h = 64
+    np.testing.assert_allclose(np.hypot(y[:, :h], y[:, h:]), np.hypot(x[:, :h], x[:, h:]), rtol=1e-12)
+    assert not np.allclose(y, x)
+
+
+def test_rope_composition_adds_angles(oracle_mod):
+    """Rotating at a then at b equals rotating at a + b."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((6, 32))
+    a = rng.integers(0, 500, 6)
+    b = rng.integers(0, 500, 6)
+    np.testing.assert_allclose(_rope(oracle_mod, _rope(oracle_mod, x, a), b), _rope(oracle_mod, x, a + b),
+                               rtol=1e-9, atol=1e-9)
+
+
+def test_rope_scores_depend_only_on_relative_position(oracle_mod):
+    """<rope(q, m), rope(k, n)> depends on m - n only -- the property the
+    rotary embedding is built for."""
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((1, 128))
+    k = rng.standard_normal((1, 128))
+    vals = []
+    for m, n in [(10, 3), (107, 100), (5007, 5000)]:
+        vals.append(float((_rope(oracle_mod, q, [m]) @ _rope(oracle_mod, k, [n]).T)[0, 0]))
+    np.testing.assert_allclose(vals, vals[0], rtol=1e-9)
+    other = float((_rope(oracle_mod, q, [11]) @ _rope(oracle_mod, k, [3]).T)[0, 0])
+    assert abs(other - vals[0]) > 1e-6
+
+
+def test_rope_append_rows_and_full_cache(oracle_mod):
+    """Each batch uses its own position; V passes through; a full cache is
+    reported (code 4)."""
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((2, 4, 16))
+    k = rng.standard_normal((2, 2, 16))
+    v = rng.standard_normal((2, 2, 16))
+    qo, ko, vo = oracle_mod.rope_append(q, k, v, [0, 9], Lmax=10)
+    assert np.array_equal(vo, v)
+    assert np.array_equal(qo[0], q[0]) and np.array_equal(ko[0], k[0])
+    np.testing.assert_allclose(ko[1], _rope(oracle_mod, k[1], [9, 9]), rtol=0, atol=0)
+    with pytest.raises(ValueError):
+        oracle_mod.rope_append(q, k, v, [0, 10], Lmax=10)
