@@ -203,6 +203,35 @@ def bench_decode_fp8(g, W, name, dev, steps, warmup, flush):
     return {"w": w, "ms": ts, "bytes": W.decode_kv_bytes_fp8(sl, w.Hkv, w.D)}
 
 
+def bench_rope_append(g, W, name, dev, steps, warmup, flush):
+    """gqa_rope_append for the new token of every sequence of decode workload
+    `name` (cache at its workload lengths); seqlens is reset before each launch
+    (outside the timed region) so every call appends at the same positions."""
+    import torch
+    w = W.WORKLOADS[name]
+    q, k, v, sl = W.make_decode_inputs(w)
+    gen = torch.Generator().manual_seed(w.seed + 100)
+    kn = torch.randn(w.B, w.Hkv, w.D, generator=gen).to(torch.bfloat16)
+    vn = torch.randn(w.B, w.Hkv, w.D, generator=gen).to(torch.bfloat16)
+    sl = (sl - 1).clamp(min=0)  # the new token becomes the last visible key
+    qd, kd, vd, knd, vnd, sl0 = (t.to(dev) for t in (q, k, v, kn, vn, sl))
+    sld = sl0.clone()
+    qo = torch.empty_like(qd)
+    stream = torch.cuda.current_stream(dev)
+
+    def prep():
+        flush()
+        sld.copy_(sl0)
+
+    ts = timed_launches(lambda: g.gqa_rope_append(qd, knd, vnd, kd, vd, sld, q_out=qo, stream=stream),
+                        steps, warmup, prep, stream)
+    flags = g.gqa_get_device_status()
+    if flags:
+        raise RuntimeError(f"rope_append {name}: device status {flags:#x}")
+    moved = 2 * (2 * w.B * w.Hq * w.D + 4 * w.B * w.Hkv * w.D) + 8 * w.B
+    return {"w": w, "ms": ts, "bytes": moved}
+
+
 def bench_prefill(g, W, dev, steps, warmup, flush):
     import torch
     w = W.WORKLOADS["prefill"]
@@ -339,6 +368,11 @@ def run_only(g, W, args, dev, flush, peaks):
         tf = r["flops"] / (ms / 1e3) / 1e12
         print(json.dumps({"only": "prefill", "us": ms * 1e3, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]}))
         return 0
+    if args.only == "rope_append":
+        r = bench_rope_append(g, W, "llama3_8b", dev, args.steps, args.warmup, flush)
+        ms = statistics.mean(r["ms"])
+        print(json.dumps({"only": "rope_append", "us": ms * 1e3, "GB/s": r["bytes"] / (ms / 1e3) / 1e9}))
+        return 0
     if args.only.endswith("_fp8"):
         r = bench_decode_fp8(g, W, args.only[:-4], dev, args.steps, args.warmup, flush)
     else:
@@ -414,6 +448,12 @@ def main():
             d8[name] = {"us": ms * 1e3, "kv_bytes_fp8": r["bytes"], "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
                         "speedup_vs_bf16": dw[name]["us"] / (ms * 1e3)}
         extras["decode_fp8_kv"] = d8
+        ra = bench_rope_append(g, W, "llama3_8b", dev, small_steps, args.warmup, flush)
+        rms = statistics.mean(ra["ms"])
+        extras["rope_append"] = {"workload": "new token of llama3_8b: B=16, Hq=32, Hkv=8, D=128, appended at 4095",
+                                 "us": rms * 1e3, "bytes_moved": ra["bytes"],
+                                 "GB/s": ra["bytes"] / (rms / 1e3) / 1e9,
+                                 "frac_hbm": ra["bytes"] / (rms / 1e3) / 1e9 / peaks["hbm_gbs"]}
         pr = bench_prefill(g, W, dev, small_steps, args.warmup, flush)
         if pr is not None:
             pms = statistics.mean(pr["ms"])

@@ -6,7 +6,7 @@ status.  All arithmetic runs in the library's CUDA kernels; there is no CPU
 or PyTorch fallback, and a missing or unloadable library raises.
 
 Names and semantics follow include/gqa.h:
-  gqa_decode, gqa_decode_fp8, gqa_prefill, gqa_decode_host, gqa_prefill_host,
+  gqa_decode, gqa_decode_fp8, gqa_rope_append, gqa_prefill, gqa_decode_host, gqa_prefill_host,
   gqa_status_string, gqa_get_device_status, gqa_decode_plan, gqa_release.
 """
 from __future__ import annotations
@@ -29,10 +29,11 @@ GQA_ERR_TOO_LARGE = 7
 GQA_DEV_SEQLEN_CLAMPED = 0x1
 GQA_DEV_EMPTY_CONTEXT = 0x2
 GQA_DEV_WAIT_TIMEOUT = 0x4
+GQA_DEV_CACHE_FULL = 0x8
 
 EXPORTED = ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host",
             "gqa_status_string", "gqa_get_device_status", "gqa_decode_plan", "gqa_release",
-            "gqa_decode_noalloc", "gqa_decode_fp8")
+            "gqa_decode_noalloc", "gqa_decode_fp8", "gqa_rope_append")
 
 _lib = None
 
@@ -58,6 +59,8 @@ def load_library():
     lib.gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.gqa_prefill_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
     lib.gqa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.gqa_rope_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_double, vp]
+    lib.gqa_rope_append.restype = i
     for fn in ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host", "gqa_decode_noalloc",
                "gqa_decode_fp8"):
         getattr(lib, fn).restype = i
@@ -158,6 +161,28 @@ def gqa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seqlens, out=None, sca
                                 _stream_ptr(stream, q.device))
     _check(st, "gqa_decode_fp8")
     return out
+
+
+def gqa_rope_append(q, k_new, v_new, k_cache, v_cache, seqlens, q_out=None, base=10000.0, stream=None):
+    """Rotary embedding of the new token at position seqlens[b] and the append
+    of its K/V heads as cache row seqlens[b]; seqlens advances by one.
+    q [B, Hq, D]; k_new, v_new [B, Hkv, D]; caches [B, Hkv, Lmax, D] (bf16,
+    device); seqlens [B] int32 (device, updated).  Returns q_out (rotated q;
+    pass q_out=q to rotate in place)."""
+    import torch
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.gqa_rope_append(_dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k_new, "k_new", torch.bfloat16),
+                                 _dev_ptr(v_new, "v_new", torch.bfloat16), _dev_ptr(q_out, "q_out", torch.bfloat16),
+                                 _dev_ptr(k_cache, "k_cache", torch.bfloat16),
+                                 _dev_ptr(v_cache, "v_cache", torch.bfloat16), _dev_ptr(seqlens, "seqlens", torch.int32),
+                                 B, Hq, Hkv, D, Lmax, float(base), _stream_ptr(stream, q.device))
+    _check(st, "gqa_rope_append")
+    return q_out
 
 
 def gqa_prefill(q, k, v, out=None, causal=True, stream=None):

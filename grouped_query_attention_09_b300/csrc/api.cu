@@ -238,6 +238,30 @@ int gqa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, cons
                        static_cast<cudaStream_t>(stream), k_scale, v_scale);
 }
 
+int gqa_rope_append(const void* q, const void* k_new, const void* v_new, void* q_out, void* k_cache,
+                    void* v_cache, int32_t* seqlens, int B, int Hq, int Hkv, int D, int Lmax, double base,
+                    void* stream) {
+  if (!q || !k_new || !v_new || !q_out || !k_cache || !v_cache || !seqlens) return GQA_ERR_NULL;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (!(base > 1.0) || !isfinite(base)) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(q_out) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+    return GQA_ERR_MISALIGNED;
+  if (!gqa::rope_supported(D)) return GQA_ERR_UNSUPPORTED;
+  DeviceCtx* c = nullptr;
+  int st;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = get_ctx(&c)) != GQA_OK) return st;
+  }
+  gqa::RopeArgs a{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_new),
+                  static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(q_out),
+                  static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache),
+                  seqlens, B, Hq, Hkv, D, Lmax, base, c->err};
+  cudaError_t e = gqa::rope_append_launch(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
 int gqa_prefill(const void* q, const void* k, const void* v, void* out, int B, int L, int Hq, int Hkv,
                 int D, int causal, void* stream) {
   int st = check_prefill_args(q, k, v, out, B, L, Hq, Hkv, D, causal);

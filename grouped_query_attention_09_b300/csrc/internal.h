@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <cuda_bf16.h>
 
 namespace gqa {
 
@@ -62,6 +63,23 @@ bool decode_tc_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, Decod
 cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream);
 
 // ------------------------------------------------------------------ prefill
+// ------------------------------------------------------------------ rope + append
+struct RopeArgs {
+  const __nv_bfloat16* q;      // [B, Hq, D]
+  const __nv_bfloat16* k_new;  // [B, Hkv, D]
+  const __nv_bfloat16* v_new;  // [B, Hkv, D]
+  __nv_bfloat16* q_out;        // [B, Hq, D] (may be q)
+  __nv_bfloat16* k_cache;      // [B, Hkv, Lmax, D]
+  __nv_bfloat16* v_cache;
+  int32_t* seqlens;            // [B], advanced by one per appended row
+  int B, Hq, Hkv, D, Lmax;
+  double base;
+  unsigned* err;
+};
+
+bool rope_supported(int D);
+cudaError_t rope_append_launch(const RopeArgs& a, cudaStream_t stream);
+
 struct PrefillArgs {
   const void* q;
   const void* k;

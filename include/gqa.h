@@ -62,6 +62,7 @@ typedef enum gqa_status {
 #define GQA_DEV_SEQLEN_CLAMPED 0x1u /* some seqlens[b] > Lmax; Lmax keys were used */
 #define GQA_DEV_EMPTY_CONTEXT 0x2u  /* some seqlens[b] <= 0; that row of out is zero */
 #define GQA_DEV_WAIT_TIMEOUT 0x4u   /* a pipeline wait gave up; results are invalid */
+#define GQA_DEV_CACHE_FULL 0x8u     /* gqa_rope_append: some seqlens[b] >= Lmax; no row appended */
 
 /*
  * gqa_decode -- one decode step: every sequence b has one new query token per
@@ -143,6 +144,38 @@ GQA_API int gqa_decode_fp8(const void* q, const void* k_cache, const void* v_cac
  */
 GQA_API int gqa_prefill(const void* q, const void* k, const void* v, void* out, int B, int L, int Hq,
                 int Hkv, int D, int causal, void* stream);
+
+/*
+ * gqa_rope_append -- the step before a decode: rotary position embedding of
+ * the new token and the append of its K/V heads to the cache.  The attention
+ * code of the GQA paper notes on 51969.com ("QA 相关") rotates the query and
+ * key heads with apply_rotary_pos_emb before repeat_kv, and the Huawei Cloud
+ * post "多头注意力机制的代码实现（MQA和GQA）", sections 2 and 5, concatenates
+ * each step's K and V to the cache; the rotation is read as the Llama "rotate
+ * half" form: for i < D/2 the pair (x[i], x[i + D/2]) turns by the angle
+ * p * base^(-2i/D), p = seqlens[b] the new token's position.
+ *
+ *   q        [B, Hq, D]          bf16, device: the new token's query heads
+ *   k_new    [B, Hkv, D]         bf16, device: its key heads (before rotation)
+ *   v_new    [B, Hkv, D]         bf16, device: its value heads
+ *   q_out    [B, Hq, D]          bf16, device: rotated query (may equal q)
+ *   k_cache, v_cache             [B, Hkv, Lmax, D] bf16, device: row p of
+ *                                (b, j) receives the rotated key / the value
+ *   seqlens  [B]                 int32, device: read as p, then set to p + 1
+ *   base     rotary base (10000 for Llama), finite and > 1
+ *
+ * Afterwards gqa_decode on q_out, the caches and seqlens attends over the new
+ * token too.  A sequence with seqlens[b] >= Lmax gets its query rotated but
+ * no row appended and its length unchanged, and GQA_DEV_CACHE_FULL is set.
+ * Angles are computed in fp64 and reduced modulo 2 pi before an fp32 sincos;
+ * the rotation itself is fp32, results rounded to bf16 (RNE).
+ *
+ * Supported: D a multiple of 16 up to 256.  Otherwise GQA_ERR_UNSUPPORTED.
+ * Allocates nothing; asynchronous on `stream`.
+ */
+GQA_API int gqa_rope_append(const void* q, const void* k_new, const void* v_new, void* q_out, void* k_cache,
+                            void* v_cache, int32_t* seqlens, int B, int Hq, int Hkv, int D, int Lmax,
+                            double base, void* stream);
 
 /*
  * gqa_decode_host / gqa_prefill_host -- the same computations on HOST
