@@ -126,6 +126,29 @@ def make_decode_fp8_inputs(w: DecodeWorkload, tail: str = "randn", q_mult: float
     return q, k8, v8, ks, vs, seqlens
 
 
+def page_cache(k, v, page_size: int, seed: int, spare_pages: int = 3):
+    """Paged copy of a contiguous cache [B, Hkv, Lmax, D]: a pool of pages
+    [num_pages, Hkv, page_size, D] (num_pages = B * ceil(Lmax / page_size) +
+    spare_pages, pages handed out in a seeded random order, spare pages left
+    as noise) and a block table [B, ceil(Lmax / page_size)] int32 with row t of
+    sequence b in page block_table[b, t // page_size], row t % page_size.
+    Rows past Lmax in a sequence's last page are padding (noise)."""
+    B, Hkv, Lmax, D = k.shape
+    mp = -(-Lmax // page_size)
+    num_pages = B * mp + spare_pages
+    g = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=g)[: B * mp].to(torch.int32)
+    bt = perm.reshape(B, mp).contiguous()
+    kp = torch.randn(num_pages, Hkv, page_size, D, generator=g).to(k.dtype)
+    vp = torch.randn(num_pages, Hkv, page_size, D, generator=g).to(v.dtype)
+    for b in range(B):
+        for i in range(mp):
+            t0, t1 = i * page_size, min((i + 1) * page_size, Lmax)
+            kp[bt[b, i], :, : t1 - t0] = k[b, :, t0:t1]
+            vp[bt[b, i], :, : t1 - t0] = v[b, :, t0:t1]
+    return kp, vp, bt
+
+
 def poison_tail(k, v, seqlens):
     """Fills cache rows t >= seqlens[b] with NaN (in place)."""
     for b in range(k.shape[0]):

@@ -62,6 +62,8 @@ def _load():
         lib.gqa_oracle_e4m3_values.restype = None
         lib.gqa_oracle_rope_append.argtypes = [p, p, p, i, p, i, i, i, i, i, ctypes.c_double, p, p, p]
         lib.gqa_oracle_rope_append.restype = i
+        lib.gqa_oracle_decode_paged.argtypes = [p, p, p, i, p, i, i, i, p, i, i, i, i, ctypes.c_double, p, i, p]
+        lib.gqa_oracle_decode_paged.restype = i
         lib.gqa_oracle_num_threads.restype = i
         _lib = lib
     return _lib
@@ -140,6 +142,31 @@ def decode_fp8(q, k8, v8, k_scale, v_scale, seqlens, scale=None, rows=None, chec
                                        B, Hq, Hkv, D, Lmax, float(scale), _ptr(r), n, _ptr(out))
     if check and rc not in (0,):
         raise ValueError(f"oracle decode_fp8 returned {rc}")
+    return out.reshape(B, Hq, D) if r is None else out
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seqlens, scale=None, rows=None, check=True):
+    """Decode over a paged cache: k_pages, v_pages [num_pages, Hkv, page_size, D];
+    block_table [B, max_pages] int (row t of sequence b is row t % page_size
+    of page block_table[b, t // page_size]); otherwise like decode()."""
+    (q, k_pages, v_pages), etype = _prep(q, k_pages, v_pages)
+    B, Hq, D = q.shape
+    num_pages, Hkv, page_size, D2 = k_pages.shape
+    if D2 != D or v_pages.shape != k_pages.shape:
+        raise ValueError("shape mismatch")
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    if bt.ndim != 2 or bt.shape[0] != B:
+        raise ValueError("block_table must be [B, max_pages]")
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32).reshape(B))
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+    n = B * Hq if r is None else r.shape[0]
+    out = np.empty((n, D), dtype=np.float64)
+    rc = _load().gqa_oracle_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), etype, _ptr(bt), num_pages, page_size,
+                                         bt.shape[1], _ptr(sl), B, Hq, Hkv, D, float(scale), _ptr(r), n, _ptr(out))
+    if check and rc != 0:
+        raise ValueError(f"oracle decode_paged returned {rc}")
     return out.reshape(B, Hq, D) if r is None else out
 
 

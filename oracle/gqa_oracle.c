@@ -231,6 +231,73 @@ int gqa_oracle_decode_fp8(const void *q, int type, const uint8_t *k8, const uint
     return rc_all;
 }
 
+/* Decode over a paged cache: the cache is a pool of pages
+ * [num_pages, Hkv, page_size, D]; row t of (b, j) is row t % page_size of
+ * page block_table[b * max_pages + t / page_size], KV head j (the split-K
+ * heuristic of the gsyq.cn page on xformers takes `page_size` and `is_paged`
+ * arguments; the page layout is this build's reading).  Everything else as
+ * gqa_oracle_decode; returns 5 if a needed page index is out of range. */
+int gqa_oracle_decode_paged(const void *q, const void *k_pages, const void *v_pages, int type,
+                            const int32_t *block_table, int num_pages, int page_size, int max_pages,
+                            const int32_t *seqlens, int B, int Hq, int Hkv, int D, double scale,
+                            const int32_t *rows, int nrows, double *out)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return 1;
+    if (num_pages <= 0 || page_size <= 0 || max_pages <= 0 || (type != 0 && type != 1)) return 1;
+    int Lcap = page_size * max_pages;
+    if (rows == NULL) nrows = B * Hq;
+    for (int b = 0; b < B; ++b)
+        if (seqlens[b] > Lcap) return 1;
+    int n_rep = Hq / Hkv;
+    int rc_all = 0;
+#pragma omp parallel
+    {
+        double *kx = malloc(sizeof(double) * (size_t)Lcap * D);
+        double *vx = malloc(sizeof(double) * (size_t)Lcap * D);
+        double *x = malloc(sizeof(double) * (size_t)Lcap);
+        double *qrow = malloc(sizeof(double) * (size_t)D);
+        int oom = !(kx && vx && x && qrow);
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < nrows; ++r) {
+            int rc = 0;
+            if (oom) {
+                rc = 2;
+            } else {
+                int b = rows ? rows[2 * r] : r / Hq;
+                int h = rows ? rows[2 * r + 1] : r % Hq;
+                if (b < 0 || b >= B || h < 0 || h >= Hq) {
+                    rc = 1;
+                } else {
+                    int n = seqlens[b] > 0 ? seqlens[b] : 0;
+                    int j = h / n_rep; /* step (2) */
+                    for (int t = 0; t < n && rc == 0; ++t) {
+                        int page = block_table[(size_t)b * max_pages + t / page_size];
+                        if (page < 0 || page >= num_pages) {
+                            rc = 5;
+                            break;
+                        }
+                        size_t base = (((size_t)page * Hkv + j) * page_size + t % page_size) * D;
+                        for (int d = 0; d < D; ++d) {
+                            kx[(size_t)t * D + d] = elem(k_pages, base + d, type);
+                            vx[(size_t)t * D + d] = elem(v_pages, base + d, type);
+                        }
+                    }
+                    if (rc == 0) {
+                        for (int d = 0; d < D; ++d) qrow[d] = elem(q, ((size_t)b * Hq + h) * D + d, type);
+                        rc = attend_row(qrow, kx, vx, n, D, scale, x, out + (size_t)r * D);
+                    }
+                }
+            }
+            if (rc) {
+#pragma omp critical
+                if (rc_all == 0 || rc < rc_all) rc_all = rc;
+            }
+        }
+        free(kx); free(vx); free(x); free(qrow);
+    }
+    return rc_all;
+}
+
 /* Exact values of n E4M3 bytes (for tests of the decoding itself). */
 void gqa_oracle_e4m3_values(const uint8_t *bytes, int n, double *out)
 {

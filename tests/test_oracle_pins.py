@@ -428,3 +428,34 @@ def test_rope_append_rows_and_full_cache(oracle_mod):
     np.testing.assert_allclose(ko[1], _rope(oracle_mod, k[1], [9, 9]), rtol=0, atol=0)
     with pytest.raises(ValueError):
         oracle_mod.rope_append(q, k, v, [0, 10], Lmax=10)
+
+
+# ---- paged cache (decode_paged) --------------------------------------------
+
+def test_decode_paged_equals_decode_on_the_gathered_cache(oracle_mod):
+    """The paged decode reads exactly the rows the block table names: it equals
+    the contiguous decode on the cache the pages were cut from, and on the
+    cache gathered back from the pool by numpy indexing (a library routine)."""
+    B, Hq, Hkv, D, Lmax, ps = 3, 8, 2, 16, 70, 32
+    g = torch.Generator().manual_seed(21)
+    q = torch.randn(B, Hq, D, generator=g, dtype=torch.float64)
+    k = torch.randn(B, Hkv, Lmax, D, generator=g, dtype=torch.float64)
+    v = torch.randn(B, Hkv, Lmax, D, generator=g, dtype=torch.float64)
+    sl = np.array([70, 1, 33], dtype=np.int32)
+    kp, vp, bt = W.page_cache(k, v, ps, seed=5)
+    paged = oracle_mod.decode_paged(q.numpy(), kp.numpy(), vp.numpy(), bt.numpy(), sl, 0.25)
+    cont = oracle_mod.decode(q.numpy(), k.numpy(), v.numpy(), sl, 0.25)
+    assert np.array_equal(paged, cont)
+    kpn, btn = kp.numpy(), bt.numpy()
+    t = np.arange(Lmax)
+    gathered = kpn[btn[:, t // ps], :, t % ps].transpose(0, 2, 1, 3)   # [B, Hkv, Lmax, D]
+    assert np.array_equal(gathered, k.numpy())
+
+
+def test_decode_paged_rejects_bad_page(oracle_mod):
+    q = np.zeros((1, 2, 8))
+    kp = np.zeros((2, 1, 4, 8))
+    bt = np.array([[0, 7]], dtype=np.int32)
+    with pytest.raises(ValueError):
+        oracle_mod.decode_paged(q, kp, kp, bt, [6])
+    oracle_mod.decode_paged(q, kp, kp, bt, [4])   # page 7 is never needed for 4 keys
