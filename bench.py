@@ -203,6 +203,25 @@ def bench_decode_fp8(g, W, name, dev, steps, warmup, flush):
     return {"w": w, "ms": ts, "bytes": W.decode_kv_bytes_fp8(sl, w.Hkv, w.D)}
 
 
+def bench_decode_paged(g, W, name, page_size, dev, steps, warmup, flush):
+    """gqa_decode_paged on workload `name` with its cache cut into pages of
+    page_size rows, handed out in a seeded random order."""
+    import torch
+    w = W.WORKLOADS[name]
+    q, k, v, sl = W.make_decode_inputs(w)
+    kp, vp, bt = W.page_cache(k, v, page_size, seed=w.seed + 50)
+    del k, v
+    qd, kd, vd, btd, sld = (t.to(dev) for t in (q, kp, vp, bt, sl))
+    out = torch.empty_like(qd)
+    stream = torch.cuda.current_stream(dev)
+    ts = timed_launches(lambda: g.gqa_decode_paged(qd, kd, vd, btd, sld, out=out, scale=w.scale, stream=stream),
+                        steps, warmup, flush, stream)
+    flags = g.gqa_get_device_status()
+    if flags:
+        raise RuntimeError(f"decode paged {name}: device status {flags:#x}")
+    return {"w": w, "ms": ts, "bytes": W.decode_kv_bytes(sl, w.Hkv, w.D)}
+
+
 def bench_rope_append(g, W, name, dev, steps, warmup, flush):
     """gqa_rope_append for the new token of every sequence of decode workload
     `name` (cache at its workload lengths); seqlens is reset before each launch
@@ -368,6 +387,13 @@ def run_only(g, W, args, dev, flush, peaks):
         tf = r["flops"] / (ms / 1e3) / 1e12
         print(json.dumps({"only": "prefill", "us": ms * 1e3, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]}))
         return 0
+    if args.only.endswith("_paged"):
+        name = args.only[:-6]
+        r = bench_decode_paged(g, W, name, 128 if name == "mqa" else 256, dev, args.steps, args.warmup, flush)
+        ms = statistics.mean(r["ms"])
+        gbs = r["bytes"] / (ms / 1e3) / 1e9
+        print(json.dumps({"only": args.only, "us": ms * 1e3, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}))
+        return 0
     if args.only == "rope_append":
         r = bench_rope_append(g, W, "llama3_8b", dev, args.steps, args.warmup, flush)
         ms = statistics.mean(r["ms"])
@@ -448,6 +474,14 @@ def main():
             d8[name] = {"us": ms * 1e3, "kv_bytes_fp8": r["bytes"], "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
                         "speedup_vs_bf16": dw[name]["us"] / (ms * 1e3)}
         extras["decode_fp8_kv"] = d8
+        dp = {}
+        for name, ps in (("llama3_8b", 256), ("mqa", 128)):
+            r = bench_decode_paged(g, W, name, ps, dev, small_steps, args.warmup, flush)
+            ms = statistics.mean(r["ms"])
+            gbs = r["bytes"] / (ms / 1e3) / 1e9
+            dp[name] = {"page_size": ps, "us": ms * 1e3, "kv_bytes": r["bytes"], "GB/s": gbs,
+                        "frac_hbm": gbs / peaks["hbm_gbs"]}
+        extras["decode_paged"] = dp
         ra = bench_rope_append(g, W, "llama3_8b", dev, small_steps, args.warmup, flush)
         rms = statistics.mean(ra["ms"])
         extras["rope_append"] = {"workload": "new token of llama3_8b: B=16, Hq=32, Hkv=8, D=128, appended at 4095",

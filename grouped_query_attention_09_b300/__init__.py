@@ -6,7 +6,7 @@ status.  All arithmetic runs in the library's CUDA kernels; there is no CPU
 or PyTorch fallback, and a missing or unloadable library raises.
 
 Names and semantics follow include/gqa.h:
-  gqa_decode, gqa_decode_fp8, gqa_rope_append, gqa_prefill, gqa_decode_host, gqa_prefill_host,
+  gqa_decode, gqa_decode_fp8, gqa_decode_paged, gqa_rope_append, gqa_prefill, gqa_decode_host, gqa_prefill_host,
   gqa_status_string, gqa_get_device_status, gqa_decode_plan, gqa_release.
 """
 from __future__ import annotations
@@ -30,10 +30,11 @@ GQA_DEV_SEQLEN_CLAMPED = 0x1
 GQA_DEV_EMPTY_CONTEXT = 0x2
 GQA_DEV_WAIT_TIMEOUT = 0x4
 GQA_DEV_CACHE_FULL = 0x8
+GQA_DEV_BAD_PAGE = 0x10
 
 EXPORTED = ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host",
             "gqa_status_string", "gqa_get_device_status", "gqa_decode_plan", "gqa_release",
-            "gqa_decode_noalloc", "gqa_decode_fp8", "gqa_rope_append")
+            "gqa_decode_noalloc", "gqa_decode_fp8", "gqa_rope_append", "gqa_decode_paged")
 
 _lib = None
 
@@ -61,6 +62,8 @@ def load_library():
     lib.gqa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.gqa_rope_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_double, vp]
     lib.gqa_rope_append.restype = i
+    lib.gqa_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.gqa_decode_paged.restype = i
     for fn in ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host", "gqa_decode_noalloc",
                "gqa_decode_fp8"):
         getattr(lib, fn).restype = i
@@ -160,6 +163,30 @@ def gqa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seqlens, out=None, sca
                                 _dev_ptr(out, "out", torch.bfloat16), B, Hq, Hkv, D, Lmax, float(scale),
                                 _stream_ptr(stream, q.device))
     _check(st, "gqa_decode_fp8")
+    return out
+
+
+def gqa_decode_paged(q, k_pages, v_pages, block_table, seqlens, out=None, scale=None, stream=None):
+    """Decode over a paged cache.  q [B, Hq, D] bf16; k_pages/v_pages
+    [num_pages, Hkv, page_size, D] bf16; block_table [B, max_pages] int32;
+    seqlens [B] int32 (all device); returns out [B, Hq, D] bf16."""
+    import torch
+    B, Hq, D = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    max_pages = block_table.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = D ** -0.5
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.gqa_decode_paged(_dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k_pages, "k_pages", torch.bfloat16),
+                                  _dev_ptr(v_pages, "v_pages", torch.bfloat16),
+                                  _dev_ptr(block_table, "block_table", torch.int32),
+                                  _dev_ptr(seqlens, "seqlens", torch.int32), _dev_ptr(out, "out", torch.bfloat16),
+                                  B, Hq, Hkv, D, num_pages, page_size, max_pages, float(scale),
+                                  _stream_ptr(stream, q.device))
+    _check(st, "gqa_decode_paged")
     return out
 
 

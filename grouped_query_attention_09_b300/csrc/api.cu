@@ -107,9 +107,14 @@ int check_prefill_args(const void* q, const void* k, const void* v, const void* 
   return GQA_OK;
 }
 
+struct PagedCache {
+  const int32_t* block_table = nullptr;
+  int page_size = 0, num_pages = 0, max_pages = 0;
+};
+
 int decode_locked(DeviceCtx& c, const void* q, const void* k, const void* v, const int32_t* seqlens,
                   void* out, int B, int Hq, int Hkv, int D, int Lmax, float scale, cudaStream_t s,
-                  const float* k_scale = nullptr, const float* v_scale = nullptr) {
+                  const float* k_scale = nullptr, const float* v_scale = nullptr, PagedCache pc = PagedCache()) {
   const bool kv8 = k_scale != nullptr;
   gqa::DecodePlan plan;
   if (!gqa::decode_plan(B, Hq, Hkv, D, Lmax, c.sm_count, &plan, 0, kv8)) return GQA_ERR_UNSUPPORTED;
@@ -134,7 +139,8 @@ int decode_locked(DeviceCtx& c, const void* q, const void* k, const void* v, con
     }
   }
   if ((e = order_after_previous(c, s)) != cudaSuccess) return cuda_fail(e);
-  gqa::DecodeArgs a{q, k, v, seqlens, out, B, Hq, Hkv, D, Lmax, scale, c.ws_part, c.counters, c.err, k_scale, v_scale};
+  gqa::DecodeArgs a{q, k, v, seqlens, out, B, Hq, Hkv, D, Lmax, scale, c.ws_part, c.counters, c.err, k_scale, v_scale,
+                    pc.block_table, pc.page_size, pc.num_pages, pc.max_pages};
   if ((e = gqa::decode_launch(plan, a, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = mark_used(c, s)) != cudaSuccess) return cuda_fail(e);
   return GQA_OK;
@@ -236,6 +242,35 @@ int gqa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, cons
   if (st != GQA_OK) return st;
   return decode_locked(*c, q, k_cache, v_cache, seqlens, out, B, Hq, Hkv, D, Lmax, scale,
                        static_cast<cudaStream_t>(stream), k_scale, v_scale);
+}
+
+int gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                     const int32_t* seqlens, void* out, int B, int Hq, int Hkv, int D, int num_pages, int page_size,
+                     int max_pages, float scale, void* stream) {
+  if (!q || !k_pages || !v_pages || !block_table || !seqlens || !out) return GQA_ERR_NULL;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_pages <= 0 || page_size <= 0 || max_pages <= 0 ||
+      Hq % Hkv != 0)
+    return GQA_ERR_INVALID_ARG;
+  if ((long long)max_pages * page_size > 0x7fffffffLL) return GQA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(seqlens) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u))
+    return GQA_ERR_MISALIGNED;
+  const int Lcap = max_pages * page_size;
+  gqa::DecodePlan plan;
+  if (!gqa::decode_plan(B, Hq, Hkv, D, Lcap, 148, &plan)) return GQA_ERR_UNSUPPORTED;
+  if (page_size % plan.tile_keys != 0) return GQA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceCtx* c = nullptr;
+  int st = get_ctx(&c);
+  if (st != GQA_OK) return st;
+  PagedCache pc;
+  pc.block_table = block_table;
+  pc.page_size = page_size;
+  pc.num_pages = num_pages;
+  pc.max_pages = max_pages;
+  return decode_locked(*c, q, k_pages, v_pages, seqlens, out, B, Hq, Hkv, D, Lcap, scale,
+                       static_cast<cudaStream_t>(stream), nullptr, nullptr, pc);
 }
 
 int gqa_rope_append(const void* q, const void* k_new, const void* v_new, void* q_out, void* k_cache,

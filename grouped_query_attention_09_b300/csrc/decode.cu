@@ -69,6 +69,8 @@ struct Params {
   float scale_log2;
   const float* k_scale;  // FP8 cache: per (b, kv head) scales of K and V
   const float* v_scale;
+  const int32_t* block_table;  // paged cache (else null): [B][max_pages] page of each logical page
+  int page_size, max_pages, num_pages;
 };
 
 struct SmemLayout {
@@ -253,6 +255,7 @@ __global__ void __launch_bounds__(288, 1)
       TileIter it;
       iter_seek(it, s_c, pre, B, Hkv);
       long long issued = 0;
+      int pg_b = -1, pg_lp = -1, pg = 0;  // last block-table entry read (paged cache)
       for (long long t = s_c; t < e_c; ++t) {
         const int i = (int)(t - s_c);
         const int s = stage_of(i);
@@ -262,7 +265,24 @@ __global__ void __launch_bounds__(288, 1)
         uint8_t* kdst = smem + s * L.stage_bytes;
         uint8_t* vdst = kdst + L.k_bytes;
         mbar_arrive_expect_tx(&full[s], L.stage_bytes);
-        const int z = it.b * Hkv + it.j, y = it.lt * kBN;
+        int z = it.b * Hkv + it.j, y = it.lt * kBN;
+        if (p.block_table) {
+          // Paged cache: logical page y / page_size of sequence b; the entry
+          // is reloaded only when the page changes.  A page index out of range
+          // is flagged and sent outside the tensor map, where TMA reads zeros.
+          const int lp = y / p.page_size;
+          if (it.b != pg_b || lp != pg_lp) {
+            pg_b = it.b;
+            pg_lp = lp;
+            pg = __ldg(p.block_table + (size_t)it.b * p.max_pages + lp);
+            if (pg < 0 || pg >= p.num_pages) {
+              atomicOr(p.err, GQA_DEV_BAD_PAGE);
+              pg = -1;
+            }
+          }
+          z = pg < 0 ? -1 : pg * Hkv + it.j;
+          y -= lp * p.page_size;
+        }
         if constexpr (KV8) {
           // one 128-byte-wide box per tensor: a row of D = 128 E4M3 bytes
           tma_load_3d(kdst, &tmK, 0, y, z, &full[s], pol);
@@ -763,11 +783,14 @@ TmapEntry g_tmap_cache[kTmapCacheSize];
 int g_tmap_n = 0, g_tmap_next = 0;
 
 cudaError_t cache_tensor_maps(const DecodeArgs& a, int D, bool kv8, CUtensorMap* tk, CUtensorMap* tv) {
-  const uint64_t pairs = (uint64_t)a.B * a.Hkv;
+  // Contiguous cache: planes (b, j) of Lmax rows; paged: planes (page, j) of page_size rows.
+  const bool paged = a.block_table != nullptr;
+  const uint64_t pairs = paged ? (uint64_t)a.num_pages * a.Hkv : (uint64_t)a.B * a.Hkv;
+  const int rows = paged ? a.page_size : a.Lmax;
   std::lock_guard<std::mutex> lk(g_tmap_mu);
   for (int e = 0; e < g_tmap_n; ++e) {
     const TmapEntry& c = g_tmap_cache[e];
-    if (c.k == a.k_cache && c.v == a.v_cache && c.D == D && c.Lmax == a.Lmax && c.pairs == pairs &&
+    if (c.k == a.k_cache && c.v == a.v_cache && c.D == D && c.Lmax == rows && c.pairs == pairs &&
         c.kv8 == (int)kv8) {
       *tk = c.tk;
       *tv = c.tv;
@@ -778,19 +801,19 @@ cudaError_t cache_tensor_maps(const DecodeArgs& a, int D, bool kv8, CUtensorMap*
   n.k = a.k_cache;
   n.v = a.v_cache;
   n.D = D;
-  n.Lmax = a.Lmax;
+  n.Lmax = rows;
   n.kv8 = (int)kv8;
   n.pairs = pairs;
   if (kv8) {
     // E4M3 bytes: one 128-byte box covers a row of D = 128 elements
-    const uint64_t s1 = (uint64_t)D, s2 = (uint64_t)a.Lmax * D;
-    if (encode_tmap_u8_3d(&n.tk, a.k_cache, D, a.Lmax, pairs, s1, s2, D, kBN, 1) != CUDA_SUCCESS ||
-        encode_tmap_u8_3d(&n.tv, a.v_cache, D, a.Lmax, pairs, s1, s2, D, kBN, 1) != CUDA_SUCCESS)
+    const uint64_t s1 = (uint64_t)D, s2 = (uint64_t)rows * D;
+    if (encode_tmap_u8_3d(&n.tk, a.k_cache, D, rows, pairs, s1, s2, D, kBN, 1) != CUDA_SUCCESS ||
+        encode_tmap_u8_3d(&n.tv, a.v_cache, D, rows, pairs, s1, s2, D, kBN, 1) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   } else {
-    const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)a.Lmax * D * 2;
-    if (encode_tmap_bf16_3d(&n.tk, a.k_cache, D, a.Lmax, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS ||
-        encode_tmap_bf16_3d(&n.tv, a.v_cache, D, a.Lmax, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS)
+    const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)rows * D * 2;
+    if (encode_tmap_bf16_3d(&n.tk, a.k_cache, D, rows, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS ||
+        encode_tmap_bf16_3d(&n.tv, a.v_cache, D, rows, pairs, s1, s2, 64, kBN, 1) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
   g_tmap_cache[g_tmap_next] = n;
@@ -826,6 +849,11 @@ cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t s
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
+  p.block_table = a.block_table;
+  p.page_size = a.page_size;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
+  if (a.block_table && (a.page_size % kBN != 0 || a.page_size <= 0)) return cudaErrorInvalidValue;
   auto kern = decode_kernel<D, NT, KV8>;
   // The opt-in shared-memory size is a per-device function attribute: set it
   // once per device to the largest size any plan can ask for.

@@ -71,6 +71,8 @@ struct TcParams {
   unsigned* err;
   int B, Hq, Hkv, G, Lmax, stages, num_ctas;
   float scale_log2;
+  const int32_t* block_table;  // paged cache (else null): [B][max_pages]
+  int page_size, max_pages, num_pages;
 };
 
 struct TcLayout {
@@ -253,9 +255,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       int seg = 0;
       long long issued = 0;
       bool ok = true;
+      int pg_b = -1, pg_lp = -1, pg = 0;  // last block-table entry read (paged cache)
       for (long long t = s_c; t < e_c && ok; ++t) {
         const long long i = t - s_c;
         const int z = it.b * Hkv + it.j;
+        int kvz = z, kvy = it.lt * kBN;
+        if (p.block_table) {
+          // Paged cache: an out-of-range page index is flagged and sent
+          // outside the tensor map, where TMA reads zeros.
+          const int lp = kvy / p.page_size;
+          if (it.b != pg_b || lp != pg_lp) {
+            pg_b = it.b;
+            pg_lp = lp;
+            pg = __ldg(p.block_table + (size_t)it.b * p.max_pages + lp);
+            if (pg < 0 || pg >= p.num_pages) {
+              atomicOr(p.err, GQA_DEV_BAD_PAGE);
+              pg = -1;
+            }
+          }
+          kvz = pg < 0 ? -1 : pg * Hkv + it.j;
+          kvy -= lp * p.page_size;
+        }
         if (t == s_c || it.lt == 0) {
           ok = mbar_wait_bounded(q_empty, (seg & 1) ^ 1, abort_flag, p.err);
           if (!ok) break;
@@ -274,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* dst = ring + s * kBlockBytes;
           const CUtensorMap* m = kv ? &tmV : &tmK;
           mbar_arrive_expect_tx(&kv_full[s], kBlockBytes);
-          tma_load_3d(dst, m, 0, it.lt * kBN, z, &kv_full[s], pol);
-          tma_load_3d(dst + kHalf, m, 64, it.lt * kBN, z, &kv_full[s], pol);
+          tma_load_3d(dst, m, 0, kvy, kvz, &kv_full[s], pol);
+          tma_load_3d(dst + kHalf, m, 64, kvy, kvz, &kv_full[s], pol);
           issued = 2 * i + kv + 1;
         }
         it_next(it, pre, B, Hkv);
@@ -648,14 +668,18 @@ cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaSt
   CUtensorMap tq, tk, tv;
   const uint64_t pairs = (uint64_t)a.B * a.Hkv;
   const int G = plan.G;
+  const bool paged = a.block_table != nullptr;
+  if (paged && (a.page_size % kBN != 0 || a.page_size <= 0)) return cudaErrorInvalidValue;
+  const uint64_t planes = paged ? (uint64_t)a.num_pages * a.Hkv : pairs;
+  const uint64_t rows = paged ? (uint64_t)a.page_size : (uint64_t)a.Lmax;
   // Q viewed as [B * Hkv][G][D]: a 128-row box starting at row 0 reads the
   // group's G heads and zero-fills rows G..127.
   if (encode_tmap_bf16_3d(&tq, a.q, kD, (uint64_t)G, pairs, (uint64_t)kD * 2, (uint64_t)G * kD * 2, 64, 128, 1) !=
           CUDA_SUCCESS ||
-      encode_tmap_bf16_3d(&tk, a.k_cache, kD, a.Lmax, pairs, (uint64_t)kD * 2, (uint64_t)a.Lmax * kD * 2, 64, kBN,
-                          1) != CUDA_SUCCESS ||
-      encode_tmap_bf16_3d(&tv, a.v_cache, kD, a.Lmax, pairs, (uint64_t)kD * 2, (uint64_t)a.Lmax * kD * 2, 64, kBN,
-                          1) != CUDA_SUCCESS)
+      encode_tmap_bf16_3d(&tk, a.k_cache, kD, rows, planes, (uint64_t)kD * 2, rows * kD * 2, 64, kBN, 1) !=
+          CUDA_SUCCESS ||
+      encode_tmap_bf16_3d(&tv, a.v_cache, kD, rows, planes, (uint64_t)kD * 2, rows * kD * 2, 64, kBN, 1) !=
+          CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   TcParams p;
   p.out = static_cast<__nv_bfloat16*>(a.out);
@@ -672,6 +696,10 @@ cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaSt
   p.stages = plan.stages;
   p.num_ctas = plan.num_ctas;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.block_table = a.block_table;
+  p.page_size = a.page_size;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
   static std::atomic<unsigned long long> attr_set{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

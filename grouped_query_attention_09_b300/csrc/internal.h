@@ -53,6 +53,12 @@ struct DecodeArgs {
   unsigned* err;      // device status word
   const float* k_scale = nullptr;  // FP8 cache: [B * Hkv] scales of K and V
   const float* v_scale = nullptr;
+  // Paged cache (block_table != nullptr): k_cache / v_cache are pools of
+  // pages [num_pages, Hkv, page_size, D]; row t of sequence b is row
+  // t % page_size of page block_table[b * max_pages + t / page_size]; Lmax is
+  // then max_pages * page_size.
+  const int32_t* block_table = nullptr;
+  int page_size = 0, num_pages = 0, max_pages = 0;
 };
 
 cudaError_t decode_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream);

@@ -63,6 +63,7 @@ typedef enum gqa_status {
 #define GQA_DEV_EMPTY_CONTEXT 0x2u  /* some seqlens[b] <= 0; that row of out is zero */
 #define GQA_DEV_WAIT_TIMEOUT 0x4u   /* a pipeline wait gave up; results are invalid */
 #define GQA_DEV_CACHE_FULL 0x8u     /* gqa_rope_append: some seqlens[b] >= Lmax; no row appended */
+#define GQA_DEV_BAD_PAGE 0x10u      /* gqa_decode_paged: a needed block-table entry is out of range; its rows read as 0 */
 
 /*
  * gqa_decode -- one decode step: every sequence b has one new query token per
@@ -144,6 +145,29 @@ GQA_API int gqa_decode_fp8(const void* q, const void* k_cache, const void* v_cac
  */
 GQA_API int gqa_prefill(const void* q, const void* k, const void* v, void* out, int B, int L, int Hq,
                 int Hkv, int D, int causal, void* stream);
+
+/*
+ * gqa_decode_paged -- gqa_decode over a paged KV cache: the cache is a pool of
+ * fixed-size pages and a block table maps each sequence's logical pages to
+ * pool pages (the split-K heuristic of the gsyq.cn page on xformers takes
+ * `page_size` and `is_paged` arguments; the layout is this library's choice).
+ *
+ *   k_pages, v_pages  [num_pages, Hkv, page_size, D]  bf16, device
+ *   block_table       [B, max_pages]  int32, device: row t of sequence b is
+ *                     row t % page_size of page block_table[b][t / page_size]
+ *   seqlens           [B] int32, device, at most max_pages * page_size
+ *                     (larger values are clamped and flagged)
+ *   everything else as gqa_decode.
+ *
+ * page_size must be a multiple of the kernel's key tile: 64 for G <= 8 (or
+ * D = 64), 128 for wider groups at D = 128.  Entries past a sequence's last
+ * page are never read; a needed entry outside [0, num_pages) sets
+ * GQA_DEV_BAD_PAGE and its rows read as zeros (never out-of-bounds memory).
+ * Supported shapes, workspace and streams as gqa_decode.
+ */
+GQA_API int gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                             const int32_t* seqlens, void* out, int B, int Hq, int Hkv, int D, int num_pages,
+                             int page_size, int max_pages, float scale, void* stream);
 
 /*
  * gqa_rope_append -- the step before a decode: rotary position embedding of
