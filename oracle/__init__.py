@@ -64,6 +64,8 @@ def _load():
         lib.gqa_oracle_rope_append.restype = i
         lib.gqa_oracle_decode_paged.argtypes = [p, p, p, i, p, i, i, i, p, i, i, i, i, ctypes.c_double, p, i, p]
         lib.gqa_oracle_decode_paged.restype = i
+        lib.gqa_oracle_prefill_chunk.argtypes = [p, p, p, i, i, i, i, i, i, i, i, ctypes.c_double, p, i, p]
+        lib.gqa_oracle_prefill_chunk.restype = i
         lib.gqa_oracle_num_threads.restype = i
         _lib = lib
     return _lib
@@ -213,3 +215,24 @@ def prefill(q, k, v, causal=True, scale=None, rows=None, check=True):
     if check and rc != 0:
         raise ValueError(f"oracle prefill returned {rc}")
     return out.reshape(B, Hq, L, D) if r is None else out
+
+
+def prefill_chunk(q, k, v, causal=True, scale=None, rows=None, check=True):
+    """Prefill of the last Lq of Lk tokens: q [B, Hq, Lq, D]; k, v [B, Hkv, Lk, D]
+    (Lk >= Lq).  Causal row i is token Lk - Lq + i and sees keys t <= Lk - Lq + i.
+    rows: optional (b, h, i) triples.  Returns fp64 [B, Hq, Lq, D] or [n, D]."""
+    (q, k, v), etype = _prep(q, k, v)
+    B, Hq, Lq, D = q.shape
+    _, Hkv, Lk, D2 = k.shape
+    if D2 != D or v.shape != k.shape or k.shape[0] != B or Lk < Lq:
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    n = B * Hq * Lq if r is None else r.shape[0]
+    out = np.empty((n, D), dtype=np.float64)
+    rc = _load().gqa_oracle_prefill_chunk(_ptr(q), _ptr(k), _ptr(v), etype, B, Lq, Lk, Hq, Hkv, D,
+                                          int(bool(causal)), float(scale), _ptr(r), n, _ptr(out))
+    if check and rc != 0:
+        raise ValueError(f"oracle prefill_chunk returned {rc}")
+    return out.reshape(B, Hq, Lq, D) if r is None else out

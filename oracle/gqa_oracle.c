@@ -414,6 +414,64 @@ int gqa_oracle_rope_append(const void *q, const void *k_new, const void *v_new, 
     return rc;
 }
 
+/* Prefill of a chunk over a cached prefix: the queries are the last Lq of
+ * Lk tokens (prefix = Lk - Lq already in the cache), k, v hold all Lk
+ * keys.  Causal: chunk row i is token prefix + i and sees keys
+ * t <= prefix + i (the square mask of the Huawei Cloud post, section 5,
+ * aligned at the bottom right, which is where a query that follows a cached
+ * prefix sits); otherwise every row sees all Lk keys.
+ *   q, out [B, Hq, Lq, D]    k, v [B, Hkv, Lk, D]
+ *   rows   (b, h, i) triples as gqa_oracle_prefill. */
+int gqa_oracle_prefill_chunk(const void *q, const void *k, const void *v, int type, int B, int Lq, int Lk,
+                             int Hq, int Hkv, int D, int causal, double scale, const int32_t *rows,
+                             int nrows, double *out)
+{
+    if (B <= 0 || Lq <= 0 || Lk < Lq || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return 1;
+    if ((causal != 0 && causal != 1) || (type != 0 && type != 1)) return 1;
+    if (rows == NULL) nrows = B * Hq * Lq;
+    int n_rep = Hq / Hkv, prefix = Lk - Lq;
+    int rc_all = 0;
+#pragma omp parallel
+    {
+        double *kx = malloc(sizeof(double) * (size_t)Lk * D);
+        double *vx = malloc(sizeof(double) * (size_t)Lk * D);
+        double *x = malloc(sizeof(double) * (size_t)Lk);
+        double *qrow = malloc(sizeof(double) * (size_t)D);
+        int oom = !(kx && vx && x && qrow);
+        int cur_b = -1, cur_h = -1;
+#pragma omp for schedule(dynamic, 16)
+        for (int r = 0; r < nrows; ++r) {
+            int rc;
+            if (oom) {
+                rc = 2;
+            } else {
+                int b = rows ? rows[3 * r] : r / (Hq * Lq);
+                int h = rows ? rows[3 * r + 1] : (r / Lq) % Hq;
+                int i = rows ? rows[3 * r + 2] : r % Lq;
+                if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= Lq) {
+                    rc = 1;
+                } else {
+                    if (b != cur_b || h != cur_h) {
+                        expand_head(k, v, type, b, h, n_rep, Hkv, Lk, D, Lk, kx, vx);
+                        cur_b = b;
+                        cur_h = h;
+                    }
+                    int n = causal ? prefix + i + 1 : Lk; /* (5), bottom-right aligned */
+                    for (int d = 0; d < D; ++d)
+                        qrow[d] = elem(q, (((size_t)b * Hq + h) * Lq + i) * D + d, type);
+                    rc = attend_row(qrow, kx, vx, n, D, scale, x, out + (size_t)r * D);
+                }
+            }
+            if (rc) {
+#pragma omp critical
+                if (rc_all == 0 || rc < rc_all) rc_all = rc;
+            }
+        }
+        free(kx); free(vx); free(x); free(qrow);
+    }
+    return rc_all;
+}
+
 int gqa_oracle_num_threads(void)
 {
 #ifdef _OPENMP

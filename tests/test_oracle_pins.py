@@ -459,3 +459,45 @@ def test_decode_paged_rejects_bad_page(oracle_mod):
     with pytest.raises(ValueError):
         oracle_mod.decode_paged(q, kp, kp, bt, [6])
     oracle_mod.decode_paged(q, kp, kp, bt, [4])   # page 7 is never needed for 4 keys
+
+
+# ---- chunked prefill over a cached prefix (prefill_chunk) -------------------
+
+def _chunk_case(seed, B=2, Hq=4, Hkv=2, Lk=23, D=8):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, Hq, Lk, D, generator=g, dtype=torch.float64)
+    k = torch.randn(B, Hkv, Lk, D, generator=g, dtype=torch.float64)
+    v = torch.randn(B, Hkv, Lk, D, generator=g, dtype=torch.float64)
+    return q.numpy(), k.numpy(), v.numpy()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_chunk_is_the_tail_of_the_full_prefill(oracle_mod, causal):
+    """Prefilling the last Lq queries over all Lk keys gives exactly the last
+    Lq rows of the full prefill (the bottom-right alignment of the mask)."""
+    q, k, v = _chunk_case(31)
+    full = oracle_mod.prefill(q, k, v, causal=causal, scale=0.4)
+    for Lq in (1, 5, 23):
+        chunk = oracle_mod.prefill_chunk(q[:, :, -Lq:], k, v, causal=causal, scale=0.4)
+        assert np.array_equal(chunk, full[:, :, -Lq:])
+
+
+def test_chunk_of_one_token_is_a_decode_step(oracle_mod):
+    q, k, v = _chunk_case(32)
+    chunk = oracle_mod.prefill_chunk(q[:, :, -1:], k, v, causal=True, scale=0.3)[:, :, 0]
+    dec = oracle_mod.decode(q[:, :, -1], k, v, [k.shape[2]] * k.shape[0], 0.3)
+    np.testing.assert_allclose(chunk, dec, rtol=1e-13, atol=1e-13)
+
+
+def test_chunk_first_row_ignores_the_chunk_after_it(oracle_mod):
+    """Row 0 of a causal chunk sees the prefix and itself only: changing the
+    later keys of the chunk leaves it unchanged."""
+    q, k, v = _chunk_case(33)
+    Lq = 9
+    a = oracle_mod.prefill_chunk(q[:, :, -Lq:], k, v, causal=True)
+    k2, v2 = k.copy(), v.copy()
+    k2[:, :, -Lq + 1:] += 5.0
+    v2[:, :, -Lq + 1:] -= 3.0
+    b = oracle_mod.prefill_chunk(q[:, :, -Lq:], k2, v2, causal=True)
+    assert np.array_equal(a[:, :, 0], b[:, :, 0])
+    assert not np.allclose(a[:, :, 1], b[:, :, 1])
