@@ -269,6 +269,22 @@ def bench_prefill(g, W, dev, steps, warmup, flush):
     return {"w": w, "ms": ts, "flops": W.prefill_flops(w.B, w.Hq, w.L, w.D, w.causal)}
 
 
+def bench_prefill_chunk(g, W, dev, steps, warmup, flush, Lq=512, Lk=2048):
+    """gqa_prefill_chunk: a chunk of Lq tokens after Lk - Lq cached ones at the
+    prefill workload's head shape (B=4, Hq=32, Hkv=8, D=128), causal."""
+    import torch
+    w = W.WORKLOADS["prefill"]
+    gen = torch.Generator().manual_seed(w.seed + 7)
+    q = torch.randn(w.B, w.Hq, Lq, w.D, generator=gen).to(torch.bfloat16).to(dev)
+    k = torch.randn(w.B, w.Hkv, Lk, w.D, generator=gen).to(torch.bfloat16).to(dev)
+    v = torch.randn(w.B, w.Hkv, Lk, w.D, generator=gen).to(torch.bfloat16).to(dev)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    ts = timed_launches(lambda: g.gqa_prefill_chunk(q, k, v, out=out, causal=True, stream=stream),
+                        steps, warmup, flush, stream)
+    return {"ms": ts, "flops": W.prefill_chunk_flops(w.B, w.Hq, Lq, Lk, w.D, True), "Lq": Lq, "Lk": Lk}
+
+
 def e2e_decode(g, W, name, steps, warmup):
     """Same metric through gqa_decode_host: pinned host inputs copied in and the
     output copied back inside the timed region, every step."""
@@ -503,6 +519,12 @@ def main():
                                                                  "prefill.cu"))}}
         else:
             extras["prefill"] = {"status": "not built"}
+        pc = bench_prefill_chunk(g, W, dev, small_steps, args.warmup, flush)
+        cms = statistics.mean(pc["ms"])
+        ctf = pc["flops"] / (cms / 1e3) / 1e12
+        extras["prefill_chunk"] = {"workload": f"causal chunk of {pc['Lq']} tokens after {pc['Lk'] - pc['Lq']} cached: "
+                                               "B=4, Hq=32, Hkv=8, D=128", "us": cms * 1e3, "flops": pc["flops"],
+                                   "TFLOP/s": ctf, "frac_tensor": ctf / peaks["bf16_tflops"]}
         if rank == 0:
             extras["e2e"] = e2e_decode(g, W, HEADLINE, steps=max(5, min(args.steps, 20)), warmup=2)
     cpu = None

@@ -6,7 +6,7 @@ status.  All arithmetic runs in the library's CUDA kernels; there is no CPU
 or PyTorch fallback, and a missing or unloadable library raises.
 
 Names and semantics follow include/gqa.h:
-  gqa_decode, gqa_decode_fp8, gqa_decode_paged, gqa_rope_append, gqa_prefill, gqa_decode_host, gqa_prefill_host,
+  gqa_decode, gqa_decode_fp8, gqa_decode_paged, gqa_rope_append, gqa_prefill, gqa_prefill_chunk, gqa_decode_host, gqa_prefill_host,
   gqa_status_string, gqa_get_device_status, gqa_decode_plan, gqa_release.
 """
 from __future__ import annotations
@@ -34,7 +34,7 @@ GQA_DEV_BAD_PAGE = 0x10
 
 EXPORTED = ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host",
             "gqa_status_string", "gqa_get_device_status", "gqa_decode_plan", "gqa_release",
-            "gqa_decode_noalloc", "gqa_decode_fp8", "gqa_rope_append", "gqa_decode_paged")
+            "gqa_decode_noalloc", "gqa_decode_fp8", "gqa_rope_append", "gqa_decode_paged", "gqa_prefill_chunk")
 
 _lib = None
 
@@ -64,6 +64,8 @@ def load_library():
     lib.gqa_rope_append.restype = i
     lib.gqa_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     lib.gqa_decode_paged.restype = i
+    lib.gqa_prefill_chunk.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+    lib.gqa_prefill_chunk.restype = i
     for fn in ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host", "gqa_decode_noalloc",
                "gqa_decode_fp8"):
         getattr(lib, fn).restype = i
@@ -225,6 +227,24 @@ def gqa_prefill(q, k, v, out=None, causal=True, stream=None):
                              _dev_ptr(v, "v", torch.bfloat16), _dev_ptr(out, "out", torch.bfloat16),
                              B, L, Hq, Hkv, D, int(bool(causal)), _stream_ptr(stream, q.device))
     _check(st, "gqa_prefill")
+    return out
+
+
+def gqa_prefill_chunk(q, k, v, out=None, causal=True, stream=None):
+    """Chunked prefill: q [B, Hq, Lq, D] (the chunk), k/v [B, Hkv, Lk, D] (the
+    cached prefix then the chunk, Lk >= Lq), bf16 on the device; causal row i
+    sees keys t <= Lk - Lq + i.  Returns out like q."""
+    import torch
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.gqa_prefill_chunk(_dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k, "k", torch.bfloat16),
+                                   _dev_ptr(v, "v", torch.bfloat16), _dev_ptr(out, "out", torch.bfloat16),
+                                   B, Lq, Lk, Hq, Hkv, D, int(bool(causal)), _stream_ptr(stream, q.device))
+    _check(st, "gqa_prefill_chunk")
     return out
 
 

@@ -311,6 +311,21 @@ int gqa_prefill(const void* q, const void* k, const void* v, void* out, int B, i
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
 }
 
+int gqa_prefill_chunk(const void* q, const void* k, const void* v, void* out, int B, int Lq, int Lk, int Hq,
+                      int Hkv, int D, int causal, void* stream) {
+  int st = check_prefill_args(q, k, v, out, B, Lq, Hq, Hkv, D, causal);
+  if (st != GQA_OK) return st;
+  if (Lk < Lq) return GQA_ERR_INVALID_ARG;
+  DeviceCtx* c = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = get_ctx(&c)) != GQA_OK) return st;
+  }
+  gqa::PrefillArgs a{q, k, v, out, B, Lq, Hq, Hkv, D, causal, c->err, Lk};
+  cudaError_t e = gqa::prefill_launch(a, c->sm_count, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
 int gqa_decode_host(const void* q_host, const void* k_cache_host, const void* v_cache_host,
                     const int32_t* seqlens_host, void* out_host, int B, int Hq, int Hkv, int D,
                     int Lmax, float scale, void* stream) {

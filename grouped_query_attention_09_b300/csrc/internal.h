@@ -91,8 +91,9 @@ struct PrefillArgs {
   const void* k;
   const void* v;
   void* out;
-  int B, L, Hq, Hkv, D, causal;
+  int B, L, Hq, Hkv, D, causal;  // L: query rows (Lq)
   unsigned* err;
+  int Lk = 0;  // key rows; 0 means L (plain prefill).  Lk > L: a chunk after Lk - L cached tokens
 };
 
 bool prefill_supported(int D);

@@ -1,5 +1,8 @@
 // prefill.cu -- causal (or full) grouped-query attention over a prompt of L
-// tokens on the tcgen05 tensor cores (row a4 of the hot path).
+// tokens on the tcgen05 tensor cores (row a4 of the hot path), and its
+// generalisation to a chunk of Lq queries that follows a cached prefix of
+// Lk - Lq tokens (Lk keys in all; the causal mask aligned at the bottom right:
+// chunk row i is token Lk - Lq + i and sees keys t <= Lk - Lq + i).
 //
 // Per head: out = softmax(QK^T / sqrt(D)) V with keys t <= i visible to query
 // i when causal (the Huawei Cloud post "多头注意力机制的代码实现（MQA和GQA）",
@@ -70,8 +73,9 @@ constexpr size_t kSmemBytes = (size_t)kOffMisc + 16 + 1024;  // + alignment slac
 
 struct Params {
   __nv_bfloat16* out;
-  int B, L, Hq, Hkv, G;
-  int nqb, nkb;     // query blocks, key blocks (both ceil(L / 128))
+  int B, Lq, Lk, Hq, Hkv, G;
+  int prefix;       // Lk - Lq: cached tokens before the first query
+  int nqb, nkb;     // query blocks ceil(Lq / 128), key blocks ceil(Lk / 128)
   int causal;
   int two;          // 1: a unit holds two heads of one group (G even)
   int per_group;    // units per (b, j, qb): G / 2 or G
@@ -95,7 +99,8 @@ __device__ __forceinline__ Unit unit_at(const Params& p, int u) {
   x.j = bj % p.Hkv;
   x.b = bj / p.Hkv;
   x.h0 = x.j * p.G + (p.two ? 2 * pr : pr);
-  x.n = p.causal ? min(x.qb + 1, p.nkb) : p.nkb;
+  // causal: keys up to the last row of the block, token prefix + min(128 qb + 127, Lq - 1)
+  x.n = p.causal ? min((p.prefix + min(x.qb * kBM + kBM - 1, p.Lq - 1)) / kBN + 1, p.nkb) : p.nkb;
   return x;
 }
 
@@ -352,8 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::pin_regs(s[2]);
         tc::pin_regs(s[3]);
         const int key0 = jb * kBN;
-        if ((p.causal && jb == x.qb) || key0 + kBN > p.L) {
-          const int lim = p.causal ? min(qi, p.L - 1) : p.L - 1;  // last visible key
+        // Mask where some key of the block lies past the first row's token
+        // (causal) or past the last key.
+        if ((p.causal && key0 + kBN - 1 > p.prefix + x.qb * kBM) || key0 + kBN > p.Lk) {
+          const int lim = p.causal ? min(p.prefix + qi, p.Lk - 1) : p.Lk - 1;  // last visible key
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -428,13 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++oc;
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.out + ((size_t)(x.b * p.Hq + h) * p.L + qi) * kD;
+      __nv_bfloat16* orow = p.out + ((size_t)(x.b * p.Hq + h) * p.Lq + qi) * kD;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
         tc::ld_32x32b_x32(o_tm + c * 32, o);
         tc::wait_ld_regs(o);
-        if (qi < p.L) {
+        if (qi < p.Lq) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
@@ -464,21 +471,25 @@ bool prefill_supported(int D) { return D == kD; }
 
 cudaError_t prefill_launch(const PrefillArgs& a, int sm_count, cudaStream_t stream) {
   if (a.D != kD) return cudaErrorNotSupported;
-  const uint64_t rowb = (uint64_t)a.D * 2, headb = (uint64_t)a.L * a.D * 2;
+  const int Lk = a.Lk > 0 ? a.Lk : a.L;
+  if (Lk < a.L) return cudaErrorInvalidValue;
+  const uint64_t rowb = (uint64_t)a.D * 2, qheadb = (uint64_t)a.L * a.D * 2, kheadb = (uint64_t)Lk * a.D * 2;
   CUtensorMap tq, tk, tv;
-  if (encode_tmap_bf16_3d(&tq, a.q, a.D, a.L, (uint64_t)a.B * a.Hq, rowb, headb, 64, kBM, 1) != CUDA_SUCCESS ||
-      encode_tmap_bf16_3d(&tk, a.k, a.D, a.L, (uint64_t)a.B * a.Hkv, rowb, headb, 64, kBN, 1) != CUDA_SUCCESS ||
-      encode_tmap_bf16_3d(&tv, a.v, a.D, a.L, (uint64_t)a.B * a.Hkv, rowb, headb, 64, kBN, 1) != CUDA_SUCCESS)
+  if (encode_tmap_bf16_3d(&tq, a.q, a.D, a.L, (uint64_t)a.B * a.Hq, rowb, qheadb, 64, kBM, 1) != CUDA_SUCCESS ||
+      encode_tmap_bf16_3d(&tk, a.k, a.D, Lk, (uint64_t)a.B * a.Hkv, rowb, kheadb, 64, kBN, 1) != CUDA_SUCCESS ||
+      encode_tmap_bf16_3d(&tv, a.v, a.D, Lk, (uint64_t)a.B * a.Hkv, rowb, kheadb, 64, kBN, 1) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   Params p;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.B = a.B;
-  p.L = a.L;
+  p.Lq = a.L;
+  p.Lk = Lk;
+  p.prefix = Lk - a.L;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.G = a.Hq / a.Hkv;
   p.nqb = (a.L + kBM - 1) / kBM;
-  p.nkb = (a.L + kBN - 1) / kBN;
+  p.nkb = (Lk + kBN - 1) / kBN;
   p.causal = a.causal;
   p.two = (p.G % 2 == 0) ? 1 : 0;
   p.per_group = p.two ? p.G / 2 : p.G;

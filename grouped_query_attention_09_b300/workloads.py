@@ -204,3 +204,10 @@ def prefill_flops(B: int, Hq: int, L: int, D: int, causal: bool) -> int:
     the causal triangle including the diagonal has L(L+1)/2 pairs per head."""
     pairs = L * (L + 1) // 2 if causal else L * L
     return 4 * B * Hq * D * pairs
+
+
+def prefill_chunk_flops(B: int, Hq: int, Lq: int, Lk: int, D: int, causal: bool) -> int:
+    """Flops of a chunk of Lq queries after Lk - Lq cached tokens: 4*D per
+    visible (query, key) pair; causal row i sees Lk - Lq + i + 1 keys."""
+    pairs = Lq * (Lk - Lq) + Lq * (Lq + 1) // 2 if causal else Lq * Lk
+    return 4 * B * Hq * D * pairs

@@ -202,6 +202,24 @@ GQA_API int gqa_rope_append(const void* q, const void* k_new, const void* v_new,
                             double base, void* stream);
 
 /*
+ * gqa_prefill_chunk -- prefill of a chunk of Lq new tokens that follows
+ * Lk - Lq tokens already in the cache (chunked prefill): the queries are the
+ * chunk's, the keys and values all Lk tokens' (prefix then chunk).  Causal:
+ * chunk row i is token Lk - Lq + i and sees keys t <= Lk - Lq + i -- the
+ * square mask of the Huawei Cloud post, section 5, aligned at the bottom
+ * right, where a query that follows a cached prefix sits; otherwise every row
+ * sees all Lk keys.  Lq == Lk is gqa_prefill.
+ *
+ *   q, out   [B, Hq, Lq, D]   bf16, device
+ *   k, v     [B, Hkv, Lk, D]  bf16, device (Lk >= Lq)
+ *
+ * Same kernel, arithmetic, scale (1/sqrt(D)) and support (D == 128) as
+ * gqa_prefill.  Allocates nothing.
+ */
+GQA_API int gqa_prefill_chunk(const void* q, const void* k, const void* v, void* out, int B, int Lq, int Lk,
+                              int Hq, int Hkv, int D, int causal, void* stream);
+
+/*
  * gqa_decode_host / gqa_prefill_host -- the same computations on HOST
  * buffers (pageable or pinned).  The call copies the inputs to library-owned
  * device buffers on `stream`, runs the device entry point, copies `out` back
