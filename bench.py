@@ -20,6 +20,10 @@ Under torchrun (N > 1) every rank runs its own batch of the same shape
 (independent sequences: no data-path collective; weak scaling); the value is
 the bytes of all ranks divided by the slowest rank's time.
 
+Also timed in the same run (reported as extra keys): FP8 (E4M3) cache decode,
+paged-cache decode, the rotary embedding + cache append of the new token, and a
+chunked prefill after a cached prefix.
+
 --impl reference times the fp64 CPU oracle on the same workload, metric and
 unit (a bounded sample of (b, h) rows, extrapolated to the full step).
 """
