@@ -55,6 +55,7 @@ constexpr int kMaxBatch = 1024;    // batches whose tile prefix fits in shared m
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448; // opt-in dynamic shared memory per CTA on sm_100-class parts
 constexpr int kMaxCtas = 160;      // persistent CTAs at most (one per SM; B300 has 148)
+constexpr float kRebase = 8.f;     // log2 units a score may exceed a head's reference max by
 
 struct Params {
   const __nv_bfloat16* q;
@@ -75,15 +76,15 @@ struct Params {
 
 struct SmemLayout {
   int stage_bytes, k_bytes;
-  int epi_off, red_off, q_off, pre_off, bar_off, flag_off, cvt_off, total;
+  int epi_off, red_off, q_off, pre_off, bar_off, flag_off, total;
 };
 
 __host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 // NG: groups of consumer warps that take alternate tiles (each group keeps
 // its own running state, merged at the end of a piece like the key slices).
-// kv8: the ring holds FP8 E4M3 tiles (one byte per element) and every tile
-// group has a private fp16 copy of its current V tile (cvt region).
+// kv8: the ring holds FP8 E4M3 tiles (one byte per element); the consumers
+// convert them in registers.
 template <int D>
 __host__ __device__ inline SmemLayout smem_layout(int stages, int Gpad, int NG, bool kv8, int G) {
   SmemLayout s;
@@ -99,9 +100,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int Gpad, int NG, 
   s.pre_off = round_up(s.q_off + Gpad * (D + 8) * 2, 16);
   s.bar_off = round_up(s.pre_off + (kMaxBatch + 1) * 4, 8);
   s.flag_off = s.bar_off + 2 * stages * 8;
-  s.cvt_off = round_up(s.flag_off + 4 * (4 + 32), 1024);
-  const int cvt_bytes = kv8 ? NG * (D / 64) * kBN * 128 : 0;  // one fp16 V tile per tile group
-  s.total = s.cvt_off + cvt_bytes + 1024;  // flags + scan scratch, fp16 copies, + slack to align the base
+  s.total = s.flag_off + 4 * (4 + 32) + 1024;  // flags + scan scratch, + slack to align the base
 
   return s;
 }
@@ -256,11 +255,21 @@ __global__ void __launch_bounds__(288, 1)
       iter_seek(it, s_c, pre, B, Hkv);
       long long issued = 0;
       int pg_b = -1, pg_lp = -1, pg = 0;  // last block-table entry read (paged cache)
+      // tile i: group ig = i % NG, use us = (i / NG) % SG of that group's
+      // ring, lap = i / (NG SG) (kept incrementally: no divisions per tile)
+      int ig = 0, us = 0, lap = 0;
       for (long long t = s_c; t < e_c; ++t) {
         const int i = (int)(t - s_c);
-        const int s = stage_of(i);
-        if (i / NG >= SG) {
-          if (!mbar_wait_bounded(&empty[s], parity_of(i) ^ 1, abort_flag, p.err)) break;
+        const int s = ig * SG + us;
+        if (lap > 0) {
+          if (!mbar_wait_bounded(&empty[s], (uint32_t)((lap - 1) & 1), abort_flag, p.err)) break;
+        }
+        if (++ig == NG) {
+          ig = 0;
+          if (++us == SG) {
+            us = 0;
+            ++lap;
+          }
         }
         uint8_t* kdst = smem + s * L.stage_bytes;
         uint8_t* vdst = kdst + L.k_bytes;
@@ -345,50 +354,59 @@ __global__ void __launch_bounds__(288, 1)
     __nv_bfloat16* q_s = reinterpret_cast<__nv_bfloat16*>(smem + L.q_off);
     constexpr int kQRow = D + 8;  // padded row (elements): rows 16 B apart in the bank map
     int seg_lt0 = 0, len_b = 0;
-    float sl_pair = p.scale_log2;  // logit scale in log2 units (times the K scale of an FP8 cache)
-    float v_mul = 1.f;             // V scale of an FP8 cache
+    // logit scale in log2 units of accumulator columns 2 (lane % 4) and + 1
+    // (an FP8 cache: times the K scale and the inverse of each head's q scale)
+    float sl_col0 = p.scale_log2, sl_col1 = p.scale_log2;
+    float v_mul = 1.f;  // V scale of an FP8 cache
     bool live = true;
 
+    // The share is walked piece by piece (a piece: the share's tiles of one
+    // (b, j) pair).  Tile i of the share (i = t - s_c) belongs to tile group
+    // i % NG; a group visits only its own tiles, so its u-th tile takes
+    // stage grp SG + u % SG with parity (u / SG) & 1, counted as it goes.
     TileIter it;
     if (s_c < e_c) iter_seek(it, s_c, pre, B, Hkv);
-    for (long long t = s_c; t < e_c; ++t) {
-      const int i = (int)(t - s_c);
-      const int s = stage_of(i);
-      const bool seg_first = (t == s_c) || (it.lt == 0);
-      const bool seg_last = (t == e_c - 1) || (it.lt == it.nb - 1);
+    int us = 0;       // u % SG
+    uint32_t ph = 0;  // (u / SG) & 1
+    long long t = s_c;
+    while (t < e_c) {
+      const int n_piece = (int)min((long long)(it.nb - it.lt), e_c - t);
       const int pair = it.b * Hkv + it.j;
 
-      if (seg_first) {
+      {
+        // ---- piece start: this pair's q, scales and a fresh running state
         seg_lt0 = it.lt;
         len_b = clamp_len(p.seqlens[it.b], p.Lmax);
-        if constexpr (KV8) {
-          sl_pair = p.scale_log2 * __ldg(p.k_scale + pair);
-          v_mul = __ldg(p.v_scale + pair);
-        }
+        if constexpr (KV8) v_mul = __ldg(p.v_scale + pair);
         const __nv_bfloat16* qb = p.q + ((size_t)it.b * p.Hq + (size_t)it.j * G) * D;
-        if constexpr (NT == 1) {
+        if constexpr (NT == 1 && !KV8) {
 #pragma unroll
           for (int kk = 0; kk < KT; ++kk) {
             const int hg = (lane >> 2);
             if (hg < G) {
-              if constexpr (KV8) {
-                // fp16, in the permuted k order of the FP8 K fragments: in
-                // k-step kk, k = 2c, 2c+1, 2c+8, 2c+9 read
-                // d = 64 (kk / 4) + 16 c + 4 (kk % 4) + 0 .. 3
-                const uint2 qv = __ldg(reinterpret_cast<const uint2*>(qb + (size_t)hg * D + 64 * (kk >> 2) +
-                                                                     16 * (lane & 3) + 4 * (kk & 3)));
-                qf[kk][0][0] = bf16x2_to_f16x2(qv.x);
-                qf[kk][0][1] = bf16x2_to_f16x2(qv.y);
-              } else {
-                const uint32_t* qp = reinterpret_cast<const uint32_t*>(qb + (size_t)hg * D + kk * 16 + 2 * (lane & 3));
-                qf[kk][0][0] = __ldg(qp);
-                qf[kk][0][1] = __ldg(qp + 4);
-              }
+              const uint32_t* qp = reinterpret_cast<const uint32_t*>(qb + (size_t)hg * D + kk * 16 + 2 * (lane & 3));
+              qf[kk][0][0] = __ldg(qp);
+              qf[kk][0][1] = __ldg(qp + 4);
             } else {
               qf[kk][0][0] = 0u;
               qf[kk][0][1] = 0u;
             }
           }
+        } else if constexpr (KV8) {
+          // fp16 q in the permuted contraction order of the FP8 K fragments
+          // (see the QK product): k-step kk, k = 2c, 2c+1 | 2c+8, 2c+9 read
+          // d = 64 (kk / 4) + 16c + 4 (kk % 4) + 0, 1 | 2, 3
+          const int hg = lane >> 2;
+#pragma unroll
+          for (int kk = 0; kk < KT; ++kk) {
+            uint2 qv = make_uint2(0u, 0u);
+            if (hg < G)
+              qv = __ldg(reinterpret_cast<const uint2*>(qb + (size_t)hg * D + 64 * (kk >> 2) + 16 * (lane & 3) +
+                                                        4 * (kk & 3)));
+            qf[kk][0][0] = pack_f16x2(__uint_as_float(qv.x << 16), __uint_as_float(qv.x & 0xFFFF0000u));
+            qf[kk][0][1] = pack_f16x2(__uint_as_float(qv.y << 16), __uint_as_float(qv.y & 0xFFFF0000u));
+          }
+          sl_col0 = sl_col1 = p.scale_log2 * __ldg(p.k_scale + pair);
         } else {
           // The previous piece's last named barrier has passed: q_s is free.
           for (int e = tid; e < G * (D / 8); e += cthreads) {
@@ -412,38 +430,44 @@ __global__ void __launch_bounds__(288, 1)
         }
       }
 
-      const bool mine = (i % NG) == grp;
-      if (live && mine) live = mbar_wait_bounded(&full[s], parity_of(i), abort_flag, p.err);
-      if (live && mine) {
+      const int first = (int)((((long long)grp - (t - s_c)) % NG + NG) % NG);
+      for (int k = first; k < n_piece; k += NG) {
+      const int lt = seg_lt0 + k;  // tile of the pair
+      const int s = grp * SG + us;
+      const uint32_t par = ph;
+      if (++us == SG) {
+        us = 0;
+        ph ^= 1u;
+      }
+      if (live) live = mbar_wait_bounded(&full[s], par, abort_flag, p.err);
+      if (live) {
         uint32_t kbase = smem_u32(smem + s * L.stage_bytes);
         uint32_t vbase = kbase + L.k_bytes;
-        const int valid = min(kBN, len_b - it.lt * kBN);  // >= 1
+        const int valid = min(kBN, len_b - lt * kBN);  // >= 1
 
+        // FP8 cache: this warp's E4M3 K bytes go to registers at the start of
+        // the tile, its V bytes before the PV product, and the stage is
+        // released once both are held (no converted copy in shared memory).
+        //   K rows g, g + 8 (g = key0 + lane / 4), 16-byte chunks c and 4 + c
+        //     (c = lane % 4): in k-step kk the fragment's k = 2c, 2c+1 | 2c+8,
+        //     2c+9 read bytes 4 (kk % 4) .. +3 of chunk 4 (kk / 4) + c -- a
+        //     permutation of the contraction index that q's fragments share;
+        //   V rows key0 + 2c, +1, +8, +9, chunk lane / 4 (d = 16 (lane / 4) ..
+        //     + 15): the A fragment of V^T in m-tile mt pairs the bytes of two
+        //     rows at columns 2 mt, 2 mt + 1 -- a permutation of the output
+        //     rows d undone when the accumulators are stored.
+        //   V rows at or past seqlens[b] read as zeros (the cache may hold
+        //   anything there, NaN included).
+        uint4 k8[2][2], v8[4];
         if constexpr (KV8) {
-          // This warp's 16 V rows, E4M3 -> fp16, into the group's fp16 tile
-          // (the layout of a bf16 tile: two 64-column halves, 128-byte rows,
-          // 16-byte chunk c of row r at chunk c ^ (r & 7)); rows at or past
-          // seqlens[b] become zeros.  Only this warp reads these rows.
-          constexpr int kTile16 = (D / 64) * kBN * 128;
-          uint8_t* vcv = smem + L.cvt_off + grp * kTile16;
-          const uint8_t* vsrc = smem + s * L.stage_bytes + L.k_bytes;
+          const uint8_t* kt = smem + s * L.stage_bytes;
+          const int g = key0 + (lane >> 2);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int e = lane + 32 * u;  // 16 rows x 8 chunks of 16 E4M3 bytes
-            const int row = key0 + (e >> 3), c = e & 7;
-            uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-            if (row < valid) {
-              const uint4 raw = *reinterpret_cast<const uint4*>(vsrc + row * 128 + ((c ^ (row & 7)) << 4));
-              lo = make_uint4(e4m3x2_to_f16x2(raw.x), e4m3x2_to_f16x2(raw.x >> 16), e4m3x2_to_f16x2(raw.y),
-                              e4m3x2_to_f16x2(raw.y >> 16));
-              hi = make_uint4(e4m3x2_to_f16x2(raw.z), e4m3x2_to_f16x2(raw.z >> 16), e4m3x2_to_f16x2(raw.w),
-                              e4m3x2_to_f16x2(raw.w >> 16));
-            }
-            uint8_t* dp = vcv + (c >> 2) * kBN * 128 + row * 128;
-            *reinterpret_cast<uint4*>(dp + ((((2 * c) & 7) ^ (row & 7)) << 4)) = lo;
-            *reinterpret_cast<uint4*>(dp + ((((2 * c + 1) & 7) ^ (row & 7)) << 4)) = hi;
+          for (int hd = 0; hd < 2; ++hd) {
+            const int ch = ((4 * hd + (lane & 3)) ^ (g & 7)) << 4;  // rows g and g + 8 share g & 7
+            k8[hd][0] = *reinterpret_cast<const uint4*>(kt + g * 128 + ch);
+            k8[hd][1] = *reinterpret_cast<const uint4*>(kt + (g + 8) * 128 + ch);
           }
-          vbase = smem_u32(vcv);
         } else if (valid < key0 + 16) {
           // Rows past the sequence end hold whatever the cache holds there
           // (possibly NaN); zero this warp's V rows so P = 0 stays 0.
@@ -466,89 +490,99 @@ __global__ void __launch_bounds__(288, 1)
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
-        uint4 k8g = make_uint4(0, 0, 0, 0), k8h = make_uint4(0, 0, 0, 0);  // E4M3 K bytes, rows g and g + 8
 #pragma unroll
-        for (int kk = 0; kk < KT; ++kk) {
-          uint32_t a[4];
-          if constexpr (KV8) {
-            // E4M3 K rows g and g + 8 of this warp's 16 keys.  One 16-byte
-            // chunk per row serves four k-steps: in k-step kk the fragment's
-            // k = 2c, 2c+1 | 2c+8, 2c+9 read bytes 4 (kk % 4) .. +3 of chunk
-            // 4 (kk / 4) + c (the q fragments use the same permutation).
-            const int g = key0 + (lane >> 2);
-            if ((kk & 3) == 0) {
-              const uint8_t* kt = smem + s * L.stage_bytes;
-              const int ch = 4 * (kk >> 2) + (lane & 3);
-              k8g = *reinterpret_cast<const uint4*>(kt + g * 128 + ((ch ^ (g & 7)) << 4));
-              k8h = *reinterpret_cast<const uint4*>(kt + (g + 8) * 128 + ((ch ^ (g & 7)) << 4));
-            }
-            const uint32_t w0 = (kk & 3) == 0 ? k8g.x : (kk & 3) == 1 ? k8g.y : (kk & 3) == 2 ? k8g.z : k8g.w;
-            const uint32_t w1 = (kk & 3) == 0 ? k8h.x : (kk & 3) == 1 ? k8h.y : (kk & 3) == 2 ? k8h.z : k8h.w;
-            a[0] = e4m3x2_to_f16x2(w0);
-            a[1] = e4m3x2_to_f16x2(w1);
-            a[2] = e4m3x2_to_f16x2(w0 >> 16);
-            a[3] = e4m3x2_to_f16x2(w1 >> 16);
-          } else {
+        float sc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // two MMA chains (even, odd k-steps)
+        if constexpr (KV8) {
+          // k-step kk: rows g and g + 8 of word kk % 4 of chunk 4 (kk / 4) + c;
+          // bytes 0, 1 are the fragment's k = 2c, 2c+1 and bytes 2, 3 its
+          // k = 2c+8, 2c+9 (the order q's fragments were loaded in)
+#pragma unroll
+          for (int kk = 0; kk < KT; ++kk) {
+            const uint4& kg = k8[kk >> 2][0];
+            const uint4& kh = k8[kk >> 2][1];
+            const uint32_t w0 = (kk & 3) == 0 ? kg.x : (kk & 3) == 1 ? kg.y : (kk & 3) == 2 ? kg.z : kg.w;
+            const uint32_t w1 = (kk & 3) == 0 ? kh.x : (kk & 3) == 1 ? kh.y : (kk & 3) == 2 ? kh.z : kh.w;
+            uint32_t a[4];
+            e4m3x4_to_f16x2x2(w0, a[0], a[2]);
+            e4m3x4_to_f16x2x2(w1, a[1], a[3]);
+            mma_f16_16816(sc2[kk & 1], a, qf[kk][0][0], qf[kk][0][1]);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[0][e] = sc2[0][e] + sc2[1][e];
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < KT; ++kk) {
+            uint32_t a[4];
             const int chunk = (kk & 3) * 2 + k_chunk_add;
             ldmatrix_x4(a, kbase + (kk >> 2) * kBN * 128 + k_row * 128 + ((chunk ^ sw) << 4));
-          }
-          if constexpr (NT == 1) {
-            if constexpr (KV8)
-              mma_f16_16816(sc[0], a, qf[kk][0][0], qf[kk][0][1]);
-            else
-              mma_bf16_16816(sc[0], a, qf[kk][0][0], qf[kk][0][1]);
-          } else {
-            // B fragments of both n-tiles for this k-step: matrices
-            // (nt, d-lo), (nt, d-hi) for nt = 0, 1; lane l addresses head
-            // row l % 8 of matrix l / 8.
-            uint32_t b[4];
-            const int m = lane >> 3;
-            const int hrow = (hs * NT + (m >> 1)) * 8 + (lane & 7);
-            ldmatrix_x4(b, smem_u32(q_s + hrow * kQRow + kk * 16 + (m & 1) * 8));
-            mma_bf16_16816(sc[0], a, b[0], b[1]);
-            mma_bf16_16816(sc[1], a, b[2], b[3]);
+            if constexpr (NT == 1) {
+              mma_bf16_16816(sc2[kk & 1], a, qf[kk][0][0], qf[kk][0][1]);
+              if (kk == KT - 1)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[0][e] = sc2[0][e] + sc2[1][e];
+            } else {
+              // B fragments of both n-tiles for this k-step: matrices
+              // (nt, d-lo), (nt, d-hi) for nt = 0, 1; lane l addresses head
+              // row l % 8 of matrix l / 8.
+              uint32_t b[4];
+              const int m = lane >> 3;
+              const int hrow = (hs * NT + (m >> 1)) * 8 + (lane & 7);
+              ldmatrix_x4(b, smem_u32(q_s + hrow * kQRow + kk * 16 + (m & 1) * 8));
+              mma_bf16_16816(sc[0], a, b[0], b[1]);
+              mma_bf16_16816(sc[1], a, b[2], b[3]);
+            }
           }
         }
 
-        if constexpr (KV8) {
-          // This warp has read its K and V rows of the E4M3 stage.
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[s]);
-        }
-
-        // ---- online softmax (log2 domain); rows = keys, columns = heads
-        const bool v_lo = key0 + (lane >> 2) < valid;
-        const bool v_hi = key0 + (lane >> 2) + 8 < valid;
+        // ---- online softmax (log2 domain); rows = keys, columns = heads.
+        // The reference point m_run of a head moves only when a score
+        // exceeds it by more than kRebase (or on the first tile), so most
+        // tiles skip the rescale of the accumulators; p stays <= 2^kRebase,
+        // and the merges below take m_run as the base of (l, acc) whatever
+        // its distance from the true maximum.
         uint32_t pb[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           float x[4];
-          x[0] = v_lo ? sc[nt][0] * sl_pair : -INFINITY;
-          x[1] = v_lo ? sc[nt][1] * sl_pair : -INFINITY;
-          x[2] = v_hi ? sc[nt][2] * sl_pair : -INFINITY;
-          x[3] = v_hi ? sc[nt][3] * sl_pair : -INFINITY;
-          float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
-#pragma unroll
-          for (int o = 4; o < 32; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+          x[0] = sc[nt][0] * sl_col0;
+          x[1] = sc[nt][1] * sl_col1;
+          x[2] = sc[nt][2] * sl_col0;
+          x[3] = sc[nt][3] * sl_col1;
+          if (valid < key0 + 16) {  // rows past the sequence end (warp-uniform test)
+            if (key0 + (lane >> 2) >= valid) x[0] = x[1] = -INFINITY;
+            if (key0 + (lane >> 2) + 8 >= valid) x[2] = x[3] = -INFINITY;
           }
-          const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
-          const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-          const float al0 = fast_exp2(m_run[nt][0] - mu0), al1 = fast_exp2(m_run[nt][1] - mu1);
-          m_run[nt][0] = mn0;
-          m_run[nt][1] = mn1;
+          // each lane tests its own scores; only a tile that moves some
+          // head's reference point pays for the column max (shuffles over
+          // the 8 lanes that share a column) and the rescale
+          float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+          if (__any_sync(0xffffffffu, mx0 > m_run[nt][0] + kRebase || mx1 > m_run[nt][1] + kRebase)) {
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+              mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+              mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+            const float al0 = fast_exp2(m_run[nt][0] - (mn0 == -INFINITY ? 0.f : mn0));
+            const float al1 = fast_exp2(m_run[nt][1] - (mn1 == -INFINITY ? 0.f : mn1));
+            m_run[nt][0] = mn0;
+            m_run[nt][1] = mn1;
+            l_run[nt][0] *= al0;
+            l_run[nt][1] *= al1;
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+              acc[kk][nt][0] *= al0;
+              acc[kk][nt][1] *= al1;
+              acc[kk][nt][2] *= al0;
+              acc[kk][nt][3] *= al1;
+            }
+          }
+          const float mu0 = m_run[nt][0] == -INFINITY ? 0.f : m_run[nt][0];
+          const float mu1 = m_run[nt][1] == -INFINITY ? 0.f : m_run[nt][1];
           const float p0 = fast_exp2(x[0] - mu0), p1 = fast_exp2(x[1] - mu1);
           const float p2 = fast_exp2(x[2] - mu0), p3 = fast_exp2(x[3] - mu1);
-          l_run[nt][0] = l_run[nt][0] * al0 + (p0 + p2);
-          l_run[nt][1] = l_run[nt][1] * al1 + (p1 + p3);
-#pragma unroll
-          for (int kk = 0; kk < KT; ++kk) {
-            acc[kk][nt][0] *= al0;
-            acc[kk][nt][1] *= al1;
-            acc[kk][nt][2] *= al0;
-            acc[kk][nt][3] *= al1;
-          }
+          l_run[nt][0] += p0 + p2;
+          l_run[nt][1] += p1 + p3;
           if constexpr (KV8) {
             pb[nt][0] = movmatrix_trans(pack_f16x2(p0, p1));
             pb[nt][1] = movmatrix_trans(pack_f16x2(p2, p3));
@@ -558,12 +592,36 @@ __global__ void __launch_bounds__(288, 1)
           }
         }
 
+        if constexpr (KV8) {
+          const uint8_t* vt = smem + s * L.stage_bytes + L.k_bytes;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int row = key0 + 2 * (lane & 3) + (r & 1) + 8 * (r >> 1);
+            v8[r] = row < valid ? *reinterpret_cast<const uint4*>(vt + row * 128 + (((lane >> 2) ^ (row & 7)) << 4))
+                                : make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+        }
         // ---- O^T += V^T P^T
 #pragma unroll
         for (int mt = 0; mt < KT; ++mt) {
           uint32_t a[4];
-          const int chunk = (mt & 3) * 2 + v_chunk_add;
-          ldmatrix_x4_trans(a, vbase + (mt >> 2) * kBN * 128 + v_row * 128 + ((chunk ^ sw) << 4));
+          if constexpr (KV8) {
+            // bytes (row 2c, row 2c+1) and (row 2c+8, row 2c+9) at columns
+            // 2 mt (m-row g) and 2 mt + 1 (m-row g + 8)
+            const int w = mt >> 1;
+            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+            const uint32_t r0 = w == 0 ? v8[0].x : w == 1 ? v8[0].y : w == 2 ? v8[0].z : v8[0].w;
+            const uint32_t r1 = w == 0 ? v8[1].x : w == 1 ? v8[1].y : w == 2 ? v8[1].z : v8[1].w;
+            const uint32_t r8 = w == 0 ? v8[2].x : w == 1 ? v8[2].y : w == 2 ? v8[2].z : v8[2].w;
+            const uint32_t r9 = w == 0 ? v8[3].x : w == 1 ? v8[3].y : w == 2 ? v8[3].z : v8[3].w;
+            e4m3x4_to_f16x2x2(__byte_perm(r0, r1, sel), a[0], a[1]);
+            e4m3x4_to_f16x2x2(__byte_perm(r8, r9, sel), a[2], a[3]);
+          } else {
+            const int chunk = (mt & 3) * 2 + v_chunk_add;
+            ldmatrix_x4_trans(a, vbase + (mt >> 2) * kBN * 128 + v_row * 128 + ((chunk ^ sw) << 4));
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             if constexpr (KV8)
@@ -575,9 +633,10 @@ __global__ void __launch_bounds__(288, 1)
         __syncwarp();
         if (!KV8 && lane == 0) mbar_arrive(&empty[s]);
       }
+      }
 
-      if (seg_last) {
-        // ---- merge the key-slice states of this piece, then output or partial
+      {
+        // ---- piece end: merge the key-slice states, then output or partial
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -594,18 +653,27 @@ __global__ void __launch_bounds__(288, 1)
           }
 #pragma unroll
           for (int mt = 0; mt < KT; ++mt) {
-            const int d = mt * 16 + (lane >> 2);
             const int hg = (hs * NT + nt) * 8 + 2 * (lane & 3);
             float* e0 = epi + (size_t)(slice * G + hg) * (D + 4);  // rows of padding heads are not kept
             float* e1 = e0 + (D + 4);
-            // (an FP8 cache's V scale is applied here, once per piece)
-            if (hg < G) {
-              e0[d] = KV8 ? acc[mt][nt][0] * v_mul : acc[mt][nt][0];
-              e0[d + 8] = KV8 ? acc[mt][nt][2] * v_mul : acc[mt][nt][2];
-            }
-            if (hg + 1 < G) {
-              e1[d] = KV8 ? acc[mt][nt][1] * v_mul : acc[mt][nt][1];
-              e1[d + 8] = KV8 ? acc[mt][nt][3] * v_mul : acc[mt][nt][3];
+            if constexpr (KV8) {
+              // m-rows g, g + 8 of m-tile mt are d = 16 g + 2 mt and + 1; the
+              // FP8 cache's V scale is applied here, once per piece
+              const int d = 16 * (lane >> 2) + 2 * mt;
+              if (hg < G)
+                *reinterpret_cast<float2*>(e0 + d) = make_float2(acc[mt][nt][0] * v_mul, acc[mt][nt][2] * v_mul);
+              if (hg + 1 < G)
+                *reinterpret_cast<float2*>(e1 + d) = make_float2(acc[mt][nt][1] * v_mul, acc[mt][nt][3] * v_mul);
+            } else {
+              const int d = mt * 16 + (lane >> 2);
+              if (hg < G) {
+                e0[d] = acc[mt][nt][0];
+                e0[d + 8] = acc[mt][nt][2];
+              }
+              if (hg + 1 < G) {
+                e1[d] = acc[mt][nt][1];
+                e1[d + 8] = acc[mt][nt][3];
+              }
             }
           }
         }
@@ -626,7 +694,7 @@ __global__ void __launch_bounds__(288, 1)
         }
         named_bar_sync(1, cthreads);
 
-        const bool complete = (seg_lt0 == 0) && (it.lt == it.nb - 1);
+        const bool complete = (seg_lt0 == 0) && (seg_lt0 + n_piece == it.nb);
         const int slot = seg_lt0 == 0 ? 1 : 0;
         const size_t slot_idx = (size_t)blockIdx.x * 2 + slot;
         __nv_bfloat16* outp = p.out + ((size_t)it.b * p.Hq + (size_t)it.j * G) * D;
@@ -760,6 +828,8 @@ __global__ void __launch_bounds__(288, 1)
         }
         named_bar_sync(1, cthreads);
       }
+      t += n_piece;
+      it.lt = seg_lt0 + n_piece - 1;  // the piece's last tile: step to the next pair
       iter_next(it, pre, B, Hkv);
     }
   }
@@ -935,7 +1005,9 @@ cudaError_t decode_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStrea
     return launch_t<128, 1, true>(plan, a, stream);
   }
   if (plan.D == 128) {
-    return plan.NT == 1 ? launch_t<128, 1, false>(plan, a, stream) : launch_t<128, 2, false>(plan, a, stream);
+    // groups wider than 8 at D = 128 run on the tcgen05 kernel (decode_plan)
+    if (plan.NT != 1) return cudaErrorInvalidValue;
+    return launch_t<128, 1, false>(plan, a, stream);
   }
   return plan.NT == 1 ? launch_t<64, 1, false>(plan, a, stream) : launch_t<64, 2, false>(plan, a, stream);
 }

@@ -146,23 +146,35 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two E4M3 values (low 16 bits of x, lower byte = first element) to an f16x2
-// (first element in the low half).  Exact: every E4M3 value is an fp16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
-  uint32_t d;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(x));
+// The two E4M3 pairs of a 32-bit word to two f16x2: bytes 0, 1 -> lo and
+// bytes 2, 3 -> hi (the halves of x are split without a shift).  Exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
+
+// Two floats to E4M3 (round to nearest even, saturating to +-448): lo -> the
+// low byte, hi -> the high byte of the result.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
   return d;
+}
+
+// D = A(16x32, row) * B(32x8, col) + C, E4M3 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// bf16x2 -> f16x2 (round to nearest; exact for values within fp16 range and precision).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
-  const float lo = __uint_as_float(x << 16), hi = __uint_as_float(x & 0xFFFF0000u);
-  return pack_f16x2(lo, hi);
 }
 
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
