@@ -65,6 +65,8 @@ def _load():
         lib.gqa_oracle_decode_paged.argtypes = [p, p, p, i, p, i, i, i, p, i, i, i, i, ctypes.c_double, p, i, p]
         lib.gqa_oracle_decode_paged.restype = i
         lib.gqa_oracle_prefill_chunk.argtypes = [p, p, p, i, i, i, i, i, i, i, i, ctypes.c_double, p, i, p]
+        lib.gqa_oracle_meanpool_heads.argtypes = [p, i, i, i, i, i, i, p]
+        lib.gqa_oracle_meanpool_heads.restype = i
         lib.gqa_oracle_prefill_chunk.restype = i
         lib.gqa_oracle_num_threads.restype = i
         _lib = lib
@@ -236,3 +238,20 @@ def prefill_chunk(q, k, v, causal=True, scale=None, rows=None, check=True):
     if check and rc != 0:
         raise ValueError(f"oracle prefill_chunk returned {rc}")
     return out.reshape(B, Hq, Lq, D) if r is None else out
+
+
+def meanpool_heads(w, Hkv, mode="mean", check=True):
+    """MHA -> GQA checkpoint conversion of a key or value projection: w
+    [H, rows, cols] (bf16 bits or fp64; the per-head blocks of the weight)
+    becomes [Hkv, rows, cols] fp64, group j's block being the mean of heads
+    j*G .. j*G + G - 1 (mode "mean") or head j*G (mode "first")."""
+    (w,), etype = _prep(w)
+    if w.ndim != 3:
+        raise ValueError("w must be [H, rows, cols]")
+    H, rows, cols = w.shape
+    out = np.empty((int(Hkv), rows, cols), dtype=np.float64)
+    m = {"mean": 0, "first": 1}[mode]
+    rc = _load().gqa_oracle_meanpool_heads(_ptr(w), etype, H, int(Hkv), rows, cols, m, _ptr(out))
+    if check and rc != 0:
+        raise ValueError(f"oracle meanpool_heads returned {rc}")
+    return out

@@ -472,6 +472,42 @@ int gqa_oracle_prefill_chunk(const void *q, const void *k, const void *v, int ty
     return rc_all;
 }
 
+/*
+ * Checkpoint conversion MHA -> GQA (the GQA paper notes on 51969.com, section
+ * "Uptraining", figure 1, and "checkpoint 转换实验", figure 4): the key (or
+ * value) projection of an H-head model is cut into its H per-head blocks
+ * w[h] (rows_per_head x cols each: the head's rows of an nn.Linear weight
+ * [H * rows_per_head, cols], or of its bias with cols = 1); group j of the
+ * GQA model with Hkv groups takes the heads h = j*G .. j*G + G - 1 (G = H /
+ * Hkv, the grouping h -> h / G of step (2)) and its block is
+ *   mode 0 ("Mean", the method the notes adopt): the mean of the G blocks,
+ *   mode 1 ("First", figure 4's comparison): the block of head j*G.
+ * Hkv = 1 is the MHA -> MQA conversion of figure 1.  out is [Hkv][rows][cols]
+ * in fp64.
+ */
+int gqa_oracle_meanpool_heads(const void *w, int type, int H, int Hkv, int rows, int cols, int mode,
+                              double *out)
+{
+    if (!w || !out || H <= 0 || Hkv <= 0 || rows <= 0 || cols <= 0 || H % Hkv != 0 || (mode != 0 && mode != 1))
+        return 1;
+    const int G = H / Hkv;
+    const size_t n = (size_t)rows * cols;
+    for (int j = 0; j < Hkv; ++j) {
+        for (size_t e = 0; e < n; ++e) {
+            double v;
+            if (mode == 1) {
+                v = elem(w, (size_t)(j * G) * n + e, type);
+            } else {
+                double sum = 0.0;
+                for (int g = 0; g < G; ++g) sum += elem(w, (size_t)(j * G + g) * n + e, type);
+                v = sum / G;
+            }
+            out[(size_t)j * n + e] = v;
+        }
+    }
+    return 0;
+}
+
 int gqa_oracle_num_threads(void)
 {
 #ifdef _OPENMP

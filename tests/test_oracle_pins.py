@@ -501,3 +501,53 @@ def test_chunk_first_row_ignores_the_chunk_after_it(oracle_mod):
     b = oracle_mod.prefill_chunk(q[:, :, -Lq:], k2, v2, causal=True)
     assert np.array_equal(a[:, :, 0], b[:, :, 0])
     assert not np.allclose(a[:, :, 1], b[:, :, 1])
+
+
+# ---- MHA -> GQA checkpoint conversion (the GQA paper notes on 51969.com,
+# "Uptraining", figures 1 and 4: each group's K/V projection head is the mean
+# of the group's heads; "First" takes the group's first head)
+def test_meanpool_is_the_group_mean_of_numpy(oracle_mod):
+    # a library routine: numpy's mean over the group axis of [Hkv, G, rows, cols]
+    w = rnd((12, 5, 7), 81)
+    for Hkv in (1, 2, 3, 4, 6, 12):
+        out = oracle_mod.meanpool_heads(w, Hkv)
+        ref = w.reshape(Hkv, 12 // Hkv, 5, 7).mean(axis=1)
+        np.testing.assert_allclose(out, ref, rtol=1e-14, atol=1e-15)
+
+
+def test_meanpool_constant_heads_closed_form(oracle_mod):
+    # head h filled with the value h: group j's block is j G + (G - 1) / 2
+    H, Hkv = 32, 8
+    G = H // Hkv
+    w = np.broadcast_to(np.arange(H, dtype=np.float64)[:, None, None], (H, 4, 6)).copy()
+    out = oracle_mod.meanpool_heads(w, Hkv)
+    for j in range(Hkv):
+        assert np.all(out[j] == j * G + (G - 1) / 2)
+
+
+def test_meanpool_identity_mqa_and_first(oracle_mod):
+    w = rnd((8, 3, 5), 82)
+    np.testing.assert_array_equal(oracle_mod.meanpool_heads(w, 8), w)  # G = 1: MHA stays MHA
+    np.testing.assert_allclose(oracle_mod.meanpool_heads(w, 1)[0], w.mean(axis=0), rtol=1e-14, atol=1e-15)
+    first = oracle_mod.meanpool_heads(w, 2, mode="first")
+    np.testing.assert_array_equal(first, w[[0, 4]])
+
+
+def test_meanpool_keys_are_the_mean_of_the_group_keys(oracle_mod):
+    # figure 1's meaning: the converted head projects x to the mean of the
+    # group's per-head keys (linearity of the projection)
+    H, Hkv, D, dm = 6, 2, 4, 10
+    w = rnd((H, D, dm), 83)
+    x = rnd((9, dm), 84)
+    out = oracle_mod.meanpool_heads(w, Hkv)
+    keys = np.einsum("nc,hdc->hnd", x, w)
+    for j in range(Hkv):
+        np.testing.assert_allclose(x @ out[j].T, keys[j * 3:(j + 1) * 3].mean(axis=0), rtol=1e-12, atol=1e-12)
+
+
+def test_meanpool_bf16_input_and_bad_args(oracle_mod):
+    bits, vals = bf16(rnd((4, 2, 8), 85))
+    bits = bits.reshape(4, 2, 8)
+    np.testing.assert_array_equal(oracle_mod.meanpool_heads(bits, 2), oracle_mod.meanpool_heads(vals, 2))
+    with pytest.raises(ValueError):
+        oracle_mod.meanpool_heads(rnd((6, 2, 2), 86), 4)  # 6 heads do not split into 4 groups
