@@ -21,8 +21,9 @@ Under torchrun (N > 1) every rank runs its own batch of the same shape
 the bytes of all ranks divided by the slowest rank's time.
 
 Also timed in the same run (reported as extra keys): FP8 (E4M3) cache decode,
-paged-cache decode, the rotary embedding + cache append of the new token, and a
-chunked prefill after a cached prefix.
+paged-cache decode, the rotary embedding + cache append of the new token, a
+chunked prefill after a cached prefix, and the MHA -> GQA mean-pool conversion
+of a K projection.
 
 --impl reference times the fp64 CPU oracle on the same workload, metric and
 unit (a bounded sample of (b, h) rows, extrapolated to the full step).
@@ -255,6 +256,18 @@ def bench_rope_append(g, W, name, dev, steps, warmup, flush):
     return {"w": w, "ms": ts, "bytes": moved}
 
 
+def bench_meanpool(g, W, dev, steps, warmup, flush, H=32, Hkv=8, D=128, d_model=4096):
+    """gqa_meanpool_kv_heads on a Llama-3-8B-shaped K projection: 32 heads of
+    [128, 4096] bf16 -> 8 groups (synthetic weights, N(0, 0.02^2))."""
+    import torch
+    gen = torch.Generator().manual_seed(77)
+    w = (torch.randn(H, D, d_model, generator=gen) * 0.02).to(torch.bfloat16).to(dev)
+    out = torch.empty(Hkv, D, d_model, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ts = timed_launches(lambda: g.gqa_meanpool_kv_heads(w, Hkv, out=out, stream=stream), steps, warmup, flush, stream)
+    return {"ms": ts, "bytes": (H + Hkv) * D * d_model * 2, "shape": (H, Hkv, D, d_model)}
+
+
 def bench_prefill(g, W, dev, steps, warmup, flush):
     import torch
     w = W.WORKLOADS["prefill"]
@@ -419,6 +432,12 @@ def run_only(g, W, args, dev, flush, peaks):
         ms = statistics.mean(r["ms"])
         print(json.dumps({"only": "rope_append", "us": ms * 1e3, "GB/s": r["bytes"] / (ms / 1e3) / 1e9}))
         return 0
+    if args.only == "kv_meanpool":
+        r = bench_meanpool(g, W, dev, args.steps, args.warmup, flush)
+        ms = statistics.mean(r["ms"])
+        gbs = r["bytes"] / (ms / 1e3) / 1e9
+        print(json.dumps({"only": "kv_meanpool", "us": ms * 1e3, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}))
+        return 0
     if args.only.endswith("_fp8"):
         r = bench_decode_fp8(g, W, args.only[:-4], dev, args.steps, args.warmup, flush)
     else:
@@ -508,6 +527,12 @@ def main():
                                  "us": rms * 1e3, "bytes_moved": ra["bytes"],
                                  "GB/s": ra["bytes"] / (rms / 1e3) / 1e9,
                                  "frac_hbm": ra["bytes"] / (rms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+        mp = bench_meanpool(g, W, dev, small_steps, args.warmup, flush)
+        mms = statistics.mean(mp["ms"])
+        extras["kv_meanpool"] = {
+            "workload": "MHA -> GQA conversion of a Llama-3-8B K projection: [32, 128, 4096] bf16 -> 8 groups",
+            "us": mms * 1e3, "bytes_moved": mp["bytes"], "GB/s": mp["bytes"] / (mms / 1e3) / 1e9,
+            "frac_hbm": mp["bytes"] / (mms / 1e3) / 1e9 / peaks["hbm_gbs"]}
         pr = bench_prefill(g, W, dev, small_steps, args.warmup, flush)
         if pr is not None:
             pms = statistics.mean(pr["ms"])

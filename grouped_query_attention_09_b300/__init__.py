@@ -34,7 +34,8 @@ GQA_DEV_BAD_PAGE = 0x10
 
 EXPORTED = ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host",
             "gqa_status_string", "gqa_get_device_status", "gqa_decode_plan", "gqa_release",
-            "gqa_decode_noalloc", "gqa_decode_fp8", "gqa_rope_append", "gqa_decode_paged", "gqa_prefill_chunk")
+            "gqa_decode_noalloc", "gqa_decode_fp8", "gqa_rope_append", "gqa_decode_paged", "gqa_prefill_chunk",
+            "gqa_meanpool_kv_heads")
 
 _lib = None
 
@@ -66,6 +67,8 @@ def load_library():
     lib.gqa_decode_paged.restype = i
     lib.gqa_prefill_chunk.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.gqa_prefill_chunk.restype = i
+    lib.gqa_meanpool_kv_heads.argtypes = [vp, vp, i, i, i, i, i, vp]
+    lib.gqa_meanpool_kv_heads.restype = i
     for fn in ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host", "gqa_decode_noalloc",
                "gqa_decode_fp8"):
         getattr(lib, fn).restype = i
@@ -212,6 +215,25 @@ def gqa_rope_append(q, k_new, v_new, k_cache, v_cache, seqlens, q_out=None, base
                                  B, Hq, Hkv, D, Lmax, float(base), _stream_ptr(stream, q.device))
     _check(st, "gqa_rope_append")
     return q_out
+
+
+def gqa_meanpool_kv_heads(w, Hkv, mode="mean", out=None, stream=None):
+    """MHA -> GQA checkpoint conversion of a key or value projection.
+    w [H, rows, cols] bf16 (device; head h's block, e.g. an nn.Linear weight
+    [H * head_dim, d_model] viewed as [H, head_dim, d_model]); returns
+    [Hkv, rows, cols]: group j's block is the mean of heads j*G .. j*G + G - 1
+    (mode "mean") or head j*G (mode "first")."""
+    import torch
+    H, rows, cols = w.shape
+    if out is None:
+        out = torch.empty((int(Hkv), rows, cols), dtype=w.dtype, device=w.device)
+    m = {"mean": 0, "first": 1}[mode]
+    lib = load_library()
+    with torch.cuda.device(w.device):
+        st = lib.gqa_meanpool_kv_heads(_dev_ptr(w, "w", torch.bfloat16), _dev_ptr(out, "out", torch.bfloat16),
+                                       H, int(Hkv), rows, cols, m, _stream_ptr(stream, w.device))
+    _check(st, "gqa_meanpool_kv_heads")
+    return out
 
 
 def gqa_prefill(q, k, v, out=None, causal=True, stream=None):

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libgqa.so")
-SOURCES = ["api.cu", "decode.cu", "decode_tc.cu", "prefill.cu", "rope.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "decode.cu", "decode_tc.cu", "prefill.cu", "rope.cu", "noalloc.cu", "convert.cu"]
 HEADERS = ["ptx.cuh", "internal.h", "tcgen05.cuh"]
 
 NVCC_FLAGS = [

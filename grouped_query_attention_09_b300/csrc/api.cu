@@ -297,6 +297,26 @@ int gqa_rope_append(const void* q, const void* k_new, const void* v_new, void* q
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
 }
 
+int gqa_meanpool_kv_heads(const void* w, void* w_out, int H, int Hkv, int rows, int cols, int mode,
+                          void* stream) {
+  if (!w || !w_out) return GQA_ERR_NULL;
+  if (H <= 0 || Hkv <= 0 || rows <= 0 || cols <= 0 || H % Hkv != 0 || (mode != 0 && mode != 1))
+    return GQA_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(w_out)) return GQA_ERR_MISALIGNED;
+  const long long n = (long long)rows * cols;
+  const char* wb = static_cast<const char*>(w);
+  const char* ob = static_cast<const char*>(w_out);
+  if (ob < wb + (size_t)H * n * 2 && wb < ob + (size_t)Hkv * n * 2) return GQA_ERR_INVALID_ARG;  // overlap
+  DeviceCtx* c = nullptr;
+  int st;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = get_ctx(&c)) != GQA_OK) return st;
+  }
+  cudaError_t e = gqa::meanpool_heads_launch(w, w_out, H, Hkv, n, mode, c->sm_count, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
 int gqa_prefill(const void* q, const void* k, const void* v, void* out, int B, int L, int Hq, int Hkv,
                 int D, int causal, void* stream) {
   int st = check_prefill_args(q, k, v, out, B, L, Hq, Hkv, D, causal);

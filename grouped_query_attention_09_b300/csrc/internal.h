@@ -86,6 +86,11 @@ struct RopeArgs {
 bool rope_supported(int D);
 cudaError_t rope_append_launch(const RopeArgs& a, cudaStream_t stream);
 
+// MHA -> GQA conversion of a K/V projection: H blocks of n bf16 values ->
+// Hkv blocks (mode 0: mean of each group's G = H / Hkv blocks; 1: its first).
+cudaError_t meanpool_heads_launch(const void* w, void* out, int H, int Hkv, long long n, int mode, int sm_count,
+                                  cudaStream_t stream);
+
 struct PrefillArgs {
   const void* q;
   const void* k;

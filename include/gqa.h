@@ -112,7 +112,7 @@ GQA_API int gqa_decode(const void* q, const void* k_cache, const void* v_cache, 
  *   k_scale, v_scale  [B, Hkv]            fp32, device (4-byte aligned)
  *   everything else as gqa_decode.
  *
- * Arithmetic: the E4M3 values are converted exactly to fp16 in shared memory;
+ * Arithmetic: the E4M3 values are converted exactly to fp16 (in registers);
  * q is rounded to fp16 (so |q| must stay below 65504), scores and softmax are
  * fp32, P is rounded to fp16, accumulation is fp32; the K scale multiplies
  * the logit scale and the V scale the output.  Cache rows at or beyond
@@ -218,6 +218,33 @@ GQA_API int gqa_rope_append(const void* q, const void* k_new, const void* v_new,
  */
 GQA_API int gqa_prefill_chunk(const void* q, const void* k, const void* v, void* out, int B, int Lq, int Lk,
                               int Hq, int Hkv, int D, int causal, void* stream);
+
+/*
+ * gqa_meanpool_kv_heads -- MHA -> GQA checkpoint conversion of one key or
+ * value projection (the GQA paper notes on 51969.com, section "Uptraining",
+ * figure 1, and the checkpoint-conversion experiment, figure 4): group j of
+ * the converted model serves query heads j*G .. j*G + G - 1 (G = H / Hkv, the
+ * h -> h / G grouping of every attention entry point here) and its K (or V)
+ * head's projection is
+ *   mode 0 ("Mean", the method the notes adopt): the mean of those G heads'
+ *          projections;
+ *   mode 1 ("First"): the projection of head j*G.
+ * Hkv == 1 is the MHA -> MQA conversion; Hkv == H copies.
+ *
+ *   w      [H, rows, cols]    bf16, device: head h's block of the projection
+ *                             (an nn.Linear weight [H * head_dim, d_model]
+ *                             viewed as [H, head_dim, d_model]; a bias with
+ *                             cols = 1)
+ *   w_out  [Hkv, rows, cols]  bf16, device, written; must not overlap w
+ *
+ * Arithmetic: fp32 sum over the group in head order, one correctly rounded
+ * division by G, bf16 round to nearest even (mode 1 copies bits).  Both
+ * pointers 16-byte aligned (else GQA_ERR_MISALIGNED); H % Hkv != 0, a mode
+ * outside {0, 1}, a non-positive size or overlapping buffers give
+ * GQA_ERR_INVALID_ARG.  Allocates nothing; asynchronous on `stream`.
+ */
+GQA_API int gqa_meanpool_kv_heads(const void* w, void* w_out, int H, int Hkv, int rows, int cols, int mode,
+                                  void* stream);
 
 /*
  * gqa_decode_host / gqa_prefill_host -- the same computations on HOST

@@ -74,6 +74,19 @@ def test_prefill_argument_errors(gqa_lib, args, status):
     assert lib.gqa_prefill(*args, None) == status
 
 
+@pytest.mark.parametrize("args,status", [
+    ((None, P, 8, 2, 4, 8, 0), 3),                                 # NULL w
+    ((P, ctypes.c_void_p(1 << 20), 8, 3, 4, 8, 0), 1),             # 8 heads into 3 groups
+    ((P, ctypes.c_void_p(1 << 20), 8, 2, 0, 8, 0), 1),             # rows = 0
+    ((P, ctypes.c_void_p(1 << 20), 8, 2, 4, 8, 2), 1),             # unknown mode
+    ((P, ctypes.c_void_p(4096 + 64), 8, 2, 4, 8, 0), 1),           # output overlaps the input
+    ((ctypes.c_void_p(4098), ctypes.c_void_p(1 << 20), 8, 2, 4, 8, 0), 4),  # w misaligned
+])
+def test_meanpool_argument_errors(gqa_lib, args, status):
+    lib = gqa_lib.load_library()
+    assert lib.gqa_meanpool_kv_heads(*args, None) == status
+
+
 def test_host_entry_points_validate_first(gqa_lib):
     lib = gqa_lib.load_library()
     assert lib.gqa_decode_host(None, P, P, P, P, 2, 8, 2, 64, 128, 0.125, None) == 3
