@@ -579,7 +579,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             // pieces' maxima, one for the weighted sums, with the loads of
             // consecutive pieces in flight together.
             const int c_lo = lf - 1, nseg = *chi_flag - c_lo + 1;
-            for (int h0 = 0; h0 < G; h0 += 32) {
+            // Up to kFastSeg pieces: every load of the thread's share is
+            // issued at once (one round trip to L2 -- the partials were
+            // written by other SMs, possibly on the other die) before any
+            // arithmetic; more pieces take the two-pass loop below.
+            constexpr int kFastSeg = 4;
+            for (int h0 = 0; h0 < G && nseg <= kFastSeg; h0 += 32) {
+              const int h = h0 + (r >> 2), cg = r & 3;
+              if (h < G) {
+                float ms[kFastSeg], ls[kFastSeg];
+                float4 x[kFastSeg][8];
+#pragma unroll
+                for (int s2 = 0; s2 < kFastSeg; ++s2) {
+                  if (s2 < nseg) {
+                    const size_t si = (size_t)(c_lo + s2) * 2 + (s2 == 0 ? 1 : 0);
+                    ms[s2] = __ldcg(p.part_ml + (si * 2 + 0) * G + h);
+                    ls[s2] = __ldcg(p.part_ml + (si * 2 + 1) * G + h);
+                    const float4* src = reinterpret_cast<const float4*>(p.part_acc + (si * G + h) * kD + cg * 32);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) x[s2][v] = __ldcg(src + v);
+                  } else {
+                    ms[s2] = -INFINITY;
+                    ls[s2] = 0.f;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) x[s2][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                  }
+                }
+                float M = ms[0];
+#pragma unroll
+                for (int s2 = 1; s2 < kFastSeg; ++s2) M = fmaxf(M, ms[s2]);
+                const float Mu = M == -INFINITY ? 0.f : M;
+                float Ls = 0.f, f[kFastSeg];
+#pragma unroll
+                for (int s2 = 0; s2 < kFastSeg; ++s2) {
+                  f[s2] = fast_exp2(ms[s2] - Mu);
+                  Ls += f[s2] * ls[s2];
+                }
+                const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+                uint4* dst = reinterpret_cast<uint4*>(outp + (size_t)h * kD + cg * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll
+                  for (int s2 = 0; s2 < kFastSeg; ++s2) {
+                    const float4 y0 = x[s2][2 * v], y1 = x[s2][2 * v + 1];
+                    a0.x += f[s2] * y0.x;
+                    a0.y += f[s2] * y0.y;
+                    a0.z += f[s2] * y0.z;
+                    a0.w += f[s2] * y0.w;
+                    a1.x += f[s2] * y1.x;
+                    a1.y += f[s2] * y1.y;
+                    a1.z += f[s2] * y1.z;
+                    a1.w += f[s2] * y1.w;
+                  }
+                  dst[v] = make_uint4(pack_bf16x2(a0.x * inv, a0.y * inv), pack_bf16x2(a0.z * inv, a0.w * inv),
+                                      pack_bf16x2(a1.x * inv, a1.y * inv), pack_bf16x2(a1.z * inv, a1.w * inv));
+                }
+              }
+            }
+            for (int h0 = 0; h0 < G && nseg > kFastSeg; h0 += 32) {
               const int h = h0 + (r >> 2), cg = r & 3;
               if (h < G) {
                 float M = -INFINITY;
