@@ -72,6 +72,7 @@ struct Params {
   const float* v_scale;
   const int32_t* block_table;  // paged cache (else null): [B][max_pages] page of each logical page
   int page_size, max_pages, num_pages;
+  int prefetch_tiles;  // > 0: one CTA per (b, kv head) pair; prefetch its first tiles into L2 at launch
 };
 
 struct SmemLayout {
@@ -195,6 +196,23 @@ __global__ void __launch_bounds__(288, 1)
   if (warp == NC && lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    // One CTA per pair (the host's choice for nearly SM-filling pair counts):
+    // when the lengths are equal this CTA's share is exactly pair blockIdx.x,
+    // so its first tiles are pulled into L2 while the prologue below reads
+    // seqlens (with unequal lengths the prefetch is merely wasted).  The rows
+    // stay inside the tensor map: at most Lmax.
+    for (int t = 0; t < p.prefetch_tiles; ++t) {
+      if constexpr (KV8) {
+        tma_prefetch_l2_3d(&tmK, 0, t * kBN, blockIdx.x);
+        tma_prefetch_l2_3d(&tmV, 0, t * kBN, blockIdx.x);
+      } else {
+#pragma unroll
+        for (int box = 0; box < D / 64; ++box) {
+          tma_prefetch_l2_3d(&tmK, box * 64, t * kBN, blockIdx.x);
+          tma_prefetch_l2_3d(&tmV, box * 64, t * kBN, blockIdx.x);
+        }
+      }
+    }
   }
 
   // ---- tile count per batch and its exclusive prefix pre[0..B] (block scan)
@@ -923,6 +941,9 @@ cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t s
   p.page_size = a.page_size;
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
+  p.prefetch_tiles = 0;
+  if (!a.block_table && plan.num_ctas == a.B * a.Hkv)
+    p.prefetch_tiles = std::min(plan.stages, (a.Lmax + kBN - 1) / kBN);
   if (a.block_table && (a.page_size % kBN != 0 || a.page_size <= 0)) return cudaErrorInvalidValue;
   auto kern = decode_kernel<D, NT, KV8>;
   // The opt-in shared-memory size is a per-device function attribute: set it
