@@ -81,6 +81,7 @@ struct RopeArgs {
   int B, Hq, Hkv, D, Lmax;
   double base;
   unsigned* err;
+  double inv_freq[128];  // base^(-2i/D), i < D/2: filled on the host by rope_append_launch
 };
 
 bool rope_supported(int D);

@@ -11,13 +11,17 @@
 // and the rotation is the Llama "rotate half" form (the pages do not spell it
 // out): for i < D/2 the pair (x[i], x[i + D/2]) turns by p * base^(-2i/D).
 //
-// One CTA per sequence: the D/2 angles are computed once in fp64 (reduced
-// modulo 2 pi before an fp32 sincos, so positions in the tens of thousands
-// keep full precision), then every thread rotates chunks of 8 pairs of the
-// query and key heads with 16-byte loads, writes the key and value rows into
-// the cache, and one thread advances seqlens[b] after a barrier.
+// One CTA per sequence: the D/2 frequencies base^(-2i/D) come in fp64 from
+// the host (the device then needs no fp64 transcendental), the angles p *
+// freq are formed and reduced modulo 2 pi in fp64 before an fp32 sincos (so
+// positions in the tens of thousands keep full precision); then every thread
+// rotates chunks of 8 pairs of the query and key heads with 16-byte loads,
+// writes the key and value rows into the cache, and one thread advances
+// seqlens[b] after a barrier.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <cmath>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -28,7 +32,7 @@ namespace {
 constexpr int kRopeThreads = 256;
 constexpr int kMaxHalf = 128;  // D <= 256
 
-__global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(RopeArgs a) {
+__global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const __grid_constant__ RopeArgs a) {
   __shared__ float cs[kMaxHalf], sn[kMaxHalf];
   __shared__ int pos_s;
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -41,9 +45,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(RopeArgs a) {
   __syncthreads();
   const int p = pos_s;
   for (int i = tid; i < half; i += kRopeThreads) {
-    const double theta = (double)p * pow(a.base, -2.0 * i / a.D);
+    const double theta = (double)p * a.inv_freq[i];
     const double two_pi = 6.283185307179586476925286766559;
-    const double r = theta - two_pi * rint(theta / two_pi);  // in [-pi, pi]
+    const double inv_two_pi = 0.15915494309189533576888376337251;
+    const double r = theta - two_pi * rint(theta * inv_two_pi);  // in [-pi, pi] up to rounding
     float s, c;
     sincosf((float)r, &s, &c);
     cs[i] = c;
@@ -106,8 +111,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(RopeArgs a) {
 
 bool rope_supported(int D) { return D >= 16 && D <= 2 * kMaxHalf && D % 16 == 0; }
 
-cudaError_t rope_append_launch(const RopeArgs& a, cudaStream_t stream) {
-  if (!rope_supported(a.D)) return cudaErrorInvalidValue;
+cudaError_t rope_append_launch(const RopeArgs& args, cudaStream_t stream) {
+  if (!rope_supported(args.D)) return cudaErrorInvalidValue;
+  RopeArgs a = args;
+  for (int i = 0; i < a.D / 2; ++i) a.inv_freq[i] = std::pow(a.base, -2.0 * i / a.D);
   rope_append_kernel<<<a.B, kRopeThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }

@@ -191,7 +191,8 @@ GQA_API int gqa_decode_paged(const void* q, const void* k_pages, const void* v_p
  * Afterwards gqa_decode on q_out, the caches and seqlens attends over the new
  * token too.  A sequence with seqlens[b] >= Lmax gets its query rotated but
  * no row appended and its length unchanged, and GQA_DEV_CACHE_FULL is set.
- * Angles are computed in fp64 and reduced modulo 2 pi before an fp32 sincos;
+ * The frequencies base^(-2i/D) are computed on the host in fp64, the angles
+ * in fp64 on the device and reduced modulo 2 pi before an fp32 sincos;
  * the rotation itself is fp32, results rounded to bf16 (RNE).
  *
  * Supported: D a multiple of 16 up to 256.  Otherwise GQA_ERR_UNSUPPORTED.
