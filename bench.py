@@ -375,6 +375,12 @@ def max_over_ranks(x, world, dev=None):
     return float(t.item())
 
 
+def job_value(bytes_per_step, world, steps, total_ms):
+    """Whole-job throughput in GB/s: every rank runs `steps` steps of its own
+    batch (weak scaling), the job takes the slowest rank's total time."""
+    return bytes_per_step * world * steps / (total_ms / 1e3) / 1e9
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -489,7 +495,7 @@ def main():
     barrier(world)
     mean_ms = statistics.mean(res["ms"])
     total_ms = max_over_ranks(sum(res["ms"]), world, dev)
-    value = res["bytes"] * world * args.steps / (total_ms / 1e3) / 1e9
+    value = job_value(res["bytes"], world, args.steps, total_ms)
     achieved = res["bytes"] / (mean_ms / 1e3) / 1e9
 
     extras = {}

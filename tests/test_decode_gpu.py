@@ -64,6 +64,31 @@ def test_many_short_sequences_complete_in_one_cta(gqa_lib, oracle_mod, cuda_devi
     assert_parity(out, oracle_decode(oracle_mod, q, k, v, sl, w.scale), "short")
 
 
+def test_one_cta_per_pair_with_unequal_lengths(gqa_lib, oracle_mod, cuda_device):
+    """128 (b, kv head) pairs nearly fill the GPU, so the plan takes one CTA per
+    pair and each CTA prefetches its pair's first tiles into L2 before it reads
+    seqlens; with unequal lengths the shares are not the pairs (the prefetch is
+    wasted) and the result must not care.  FP8 cache too."""
+    B, Hq, Hkv, D, Lmax = 16, 32, 8, 128, 1024
+    tk, ctas = gqa_lib.gqa_decode_plan(B, Hq, Hkv, D, Lmax)
+    assert ctas == B * Hkv
+    w = W.DecodeWorkload("pairs", B, Hq, Hkv, D, Lmax, 1, Lmax, 4242)
+    q, k, v, _ = W.make_decode_inputs(w)
+    sl = torch.tensor([1024, 1, 700, 65, 64, 1000, 3, 512, 1024, 129, 900, 2, 640, 33, 1023, 256],
+                      dtype=torch.int32)
+    out, flags = run_decode(gqa_lib, q, k, v, sl, w.scale, cuda_device)
+    assert flags == 0
+    assert_parity(out, oracle_decode(oracle_mod, q, k, v, sl, w.scale), "one CTA per pair, unequal")
+    k8, v8, ks, vs = W.quantize_kv_fp8(k, v)
+    dev = cuda_device
+    out8 = gqa_lib.gqa_decode_fp8(q.to(dev), k8.to(dev), v8.to(dev), ks.to(dev), vs.to(dev), sl.to(dev),
+                                  scale=w.scale)
+    assert gqa_lib.gqa_get_device_status() == 0
+    ref8 = oracle_mod.decode_fp8(W.bf16_bits(q), k8.numpy(), v8.numpy(), ks.numpy(), vs.numpy(), sl.numpy(),
+                                 scale=w.scale)
+    assert_parity(out8.double().cpu().numpy(), ref8, "fp8, one CTA per pair, unequal")
+
+
 def test_nan_tail_is_never_read(gqa_lib, oracle_mod, cuda_device):
     """Cache rows past seqlens[b] filled with NaN (the poison test): the kernel
     must neither read them into a score nor let 0 * NaN into P V."""
