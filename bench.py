@@ -51,8 +51,8 @@ HEADLINE = "llama3_8b"
 # SHA-256 of the kernel source they were taken on; reported as null as soon
 # as the source differs.
 NCU_TRAFFIC = {
-    "decode.cu": {"sha256": "2ba40d1a7e07926c94877a103f054158df78d02cdfad3ecfa1000be1c1b394c9",
-                  "bytes_per_launch": 271520768.0,
+    "decode.cu": {"sha256": "e8d952e93c0637b010515cf85169bcda61e1c5e3c2b1c22700e0e01f18df403d",
+                  "bytes_per_launch": 271471104.0,
                   "capture": "ncu --set full, llama3_8b decode (dram__bytes_read.sum + dram__bytes_write.sum)"},
     "prefill.cu": {"sha256": "fde18f28b4183cbe75a94a0a460551387325fe5c0c35e2952fa39aea5208a574",
                    "bytes_per_launch": 115401216.0,
