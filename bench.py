@@ -54,9 +54,9 @@ NCU_TRAFFIC = {
     "decode.cu": {"sha256": "e8d952e93c0637b010515cf85169bcda61e1c5e3c2b1c22700e0e01f18df403d",
                   "bytes_per_launch": 271471104.0,
                   "capture": "ncu --set full, llama3_8b decode (dram__bytes_read.sum + dram__bytes_write.sum)"},
-    "prefill.cu": {"sha256": "fde18f28b4183cbe75a94a0a460551387325fe5c0c35e2952fa39aea5208a574",
-                   "bytes_per_launch": 115401216.0,
-                   "capture": "ncu --set full, causal prefill B=4 L=2048 (dram__bytes_read.sum + dram__bytes_write.sum)"},
+    "prefill.cu": {"sha256": "ca3f3d65e2542ced2179f6472590ec6bd394e80cff71a988b85ce30b2ae7cd17",
+                   "bytes_per_launch": 115492864.0,
+                   "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, causal prefill B=4 L=2048"},
 }
 
 

@@ -43,6 +43,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -498,14 +499,14 @@ cudaError_t prefill_launch(const PrefillArgs& a, int sm_count, cudaStream_t stre
   p.units = (int)units;
   p.scale_log2 = (1.0f / sqrtf((float)a.D)) * 1.4426950408889634f;
   p.err = a.err;
-  static unsigned long long attr_set = 0;  // one bit per device ordinal < 64
+  static std::atomic<unsigned long long> attr_set{0};  // one bit per device ordinal < 64
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(attr_set >> dev & 1ull)) {
+  if (dev >= 64 || !(attr_set.load() >> dev & 1ull)) {
     e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set |= 1ull << dev;
+    if (dev < 64) attr_set.fetch_or(1ull << dev);
   }
   const int grid = (int)std::min<long long>(units, sm_count);
   prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
