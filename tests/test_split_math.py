@@ -75,3 +75,55 @@ def test_tile_groups_never_share_a_stage():
         # the producer's drain: the last NG*SG tiles cover every stage once
         for issued in range(NG * SG, 60):
             assert sorted(stage_of(i, NG, SG) for i in range(issued - NG * SG, issued)) == list(range(NG * SG))
+
+
+def test_incremental_counters_match_the_closed_form():
+    """The decode kernel keeps the ring position incrementally instead of
+    dividing per tile.  Producer: (ig, us, lap) advance once per tile; tile i
+    goes to stage ig*SG + us and, once lap > 0, first waits for the stage's
+    previous use with parity (lap - 1) & 1.  Consumers: each tile group walks
+    only its own tiles, piece by piece (a piece: the share's tiles of one
+    (b, kv head) pair), starting at offset (grp - i0) mod NG of a piece that
+    begins at share index i0, and keeps (us, ph) per own tile.  Both must name
+    the closed-form stage and parity of every tile, for any cut into pieces."""
+    import random
+    rng = random.Random(7)
+    for NG, stages in [(1, 2), (1, 6), (2, 4), (2, 6), (2, 8), (3, 9), (3, 12)]:
+        SG = stages // NG
+        for trial in range(40):
+            n = rng.randint(1, 120)
+            # producer
+            ig = us = lap = 0
+            for i in range(n):
+                s = ig * SG + us
+                assert s == stage_of(i, NG, SG)
+                if lap > 0:
+                    assert (lap - 1) & 1 == parity_of(i - NG * SG, NG, SG)
+                else:
+                    assert i // NG < SG
+                ig += 1
+                if ig == NG:
+                    ig = 0
+                    us += 1
+                    if us == SG:
+                        us = 0
+                        lap += 1
+            # consumers, over a random cut of the share into pieces
+            cuts = sorted(rng.sample(range(1, n), min(n - 1, rng.randint(0, 6)))) if n > 1 else []
+            bounds = [0] + cuts + [n]
+            for grp in range(NG):
+                us = ph = 0
+                seen = []
+                for i0, i1 in zip(bounds, bounds[1:]):
+                    first = ((grp - i0) % NG + NG) % NG
+                    for k in range(first, i1 - i0, NG):
+                        i = i0 + k
+                        assert i % NG == grp
+                        assert grp * SG + us == stage_of(i, NG, SG)
+                        assert ph == parity_of(i, NG, SG)
+                        seen.append(i)
+                        us += 1
+                        if us == SG:
+                            us = 0
+                            ph ^= 1
+                assert seen == [i for i in range(n) if i % NG == grp]
