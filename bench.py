@@ -51,9 +51,9 @@ HEADLINE = "llama3_8b"
 # SHA-256 of the kernel source they were taken on; reported as null as soon
 # as the source differs.
 NCU_TRAFFIC = {
-    "decode.cu": {"sha256": "e8d952e93c0637b010515cf85169bcda61e1c5e3c2b1c22700e0e01f18df403d",
+    "decode.cu": {"sha256": "6bc09f83fdc88f2a3bf61d049203c56191f4dcbfd946d6a7f6a5758156894249",
                   "bytes_per_launch": 271471104.0,
-                  "capture": "ncu --set full, llama3_8b decode (dram__bytes_read.sum + dram__bytes_write.sum)"},
+                  "capture": "ncu --set full, llama3_8b decode (dram__bytes_read.sum + dram__bytes_write.sum); the source changed since only in comments (identical cubin)"},
     "prefill.cu": {"sha256": "ca3f3d65e2542ced2179f6472590ec6bd394e80cff71a988b85ce30b2ae7cd17",
                    "bytes_per_launch": 115492864.0,
                    "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, causal prefill B=4 L=2048"},

@@ -24,16 +24,22 @@
 // CTA layout: warps 0..NC-1 consume, warp NC produces.
 //   producer: one lane streams K and V tiles [tile_keys x D] of the cache into
 //     a ring of shared-memory stages with 3-D TMA loads (128-byte swizzle,
-//     evict-first L2 policy), an mbarrier pair per stage;
-//   consumers: a 4 x HS grid of warps; warp (ks, hs) owns keys
-//     [16 ks, 16 ks + 16) of every tile and query heads [8 NT hs, 8 NT (hs+1))
-//     of the group.  Scores are computed transposed, S^T = K q^T, with
-//     mma.sync m16n8k16 (keys in M, heads in N, D in K); the online softmax
-//     runs on the accumulator fragments (per-head max over keys by warp
-//     shuffles); P^T is turned into the B operand of O^T = V^T P^T with
-//     movmatrix; V^T comes from the swizzled V tile through ldmatrix.trans.
-//     The four key-slice states of a head are merged in shared memory at the
-//     end of each piece.
+//     evict-first L2 policy), an mbarrier pair per stage; with one CTA per
+//     (b, kv head) pair it first prefetches the pair's opening tiles into L2
+//     while the prologue reads seqlens;
+//   consumers: NG tile groups (two for G <= 8) of a 4 x HS grid of warps take
+//     alternate tiles, each group from a private part of the ring and walking
+//     only its own tiles; warp (ks, hs) owns keys [16 ks, 16 ks + 16) of its
+//     group's tiles and query heads [8 NT hs, 8 NT (hs+1)) of the group.
+//     Scores are computed transposed, S^T = K q^T, with mma.sync m16n8k16
+//     (keys in M, heads in N, D in K); the online softmax runs on the
+//     accumulator fragments, with a per-head reference max that moves only
+//     when a score passes it by more than 2^8 (then the column max by warp
+//     shuffles and the rescale); P^T is turned into the B operand of
+//     O^T = V^T P^T with movmatrix; V^T comes from the swizzled V tile through
+//     ldmatrix.trans (an FP8 cache: both come from E4M3 bytes converted in
+//     registers).  The key-slice states of a head are merged in shared memory
+//     at the end of each piece.
 //   Decode intensity is G flop per cache byte (<= 64), far below the tensor
 //   ridge point, so the warp-level MMA is not the bound; HBM is.
 #include <cuda_bf16.h>
