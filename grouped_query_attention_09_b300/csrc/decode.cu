@@ -1007,9 +1007,14 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
     // equal lengths every share is then exactly one pair, so no pair is cut
     // and no cross-CTA merge runs (each SM's ring still keeps its share of
     // HBM bandwidth in flight).  Ragged lengths are still balanced by the
-    // tile split, at the cost of some cuts.
+    // tile split, at the cost of some cuts.  Short caches (at most 8 tiles
+    // per pair) also take one CTA per pair: a cut would save less time than
+    // the merge it adds (a partial write, an arrival atomic and a chain of
+    // L2 reads).
     const long long pairs = (long long)B * Hkv;
-    if (pairs <= plan->num_ctas && pairs * 4 >= (long long)plan->num_ctas * 3) plan->num_ctas = (int)pairs;
+    const long long tiles_per_pair = (Lmax + kBN - 1) / kBN;
+    if (pairs <= plan->num_ctas && (pairs * 4 >= (long long)plan->num_ctas * 3 || tiles_per_pair <= 8))
+      plan->num_ctas = (int)pairs;
   }
   SmemLayout l0 = D == 64 ? smem_layout<64>(0, Gpad, NG, kv8, G) : smem_layout<128>(0, Gpad, NG, kv8, G);
   int stages = std::min(kMaxStages, (kSmemLimit - l0.total - 2 * kMaxStages * 8) / l0.stage_bytes);

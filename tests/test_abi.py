@@ -95,7 +95,7 @@ def test_host_entry_points_validate_first(gqa_lib):
 
 
 @pytest.mark.parametrize("shape,tile_keys,ctas", [
-    ((2, 8, 2, 64, 128), 64, 8),          # 4 (b, kv head) pairs x 2 tiles of 64 keys
+    ((2, 8, 2, 64, 128), 64, 4),          # 4 short pairs (2 tiles of 64 keys): one CTA each, no cut
     ((16, 32, 8, 128, 4096), 64, 128),    # 128 pairs nearly fill 148 SMs: one CTA per pair
     ((8, 64, 8, 128, 16384), 64, 148),
     ((64, 32, 1, 128, 2048), 128, 148),   # G = 32: tcgen05 kernel, 128-key blocks
