@@ -464,7 +464,9 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="headline only (for profiling runs)")
-    ap.add_argument("--only", default=None, help="time one workload (a decode name or 'prefill') and print its line")
+    ap.add_argument("--only", default=None,
+                    help="time one workload and print its line: a decode workload name (tiny, llama3_8b, "
+                         "llama2_70b, mqa), optionally with _fp8 or _paged; prefill; rope_append; kv_meanpool")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
