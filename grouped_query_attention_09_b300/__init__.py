@@ -7,7 +7,9 @@ or PyTorch fallback, and a missing or unloadable library raises.
 
 Names and semantics follow include/gqa.h:
   gqa_decode, gqa_decode_fp8, gqa_decode_paged, gqa_rope_append, gqa_prefill, gqa_prefill_chunk, gqa_decode_host, gqa_prefill_host,
-  gqa_status_string, gqa_get_device_status, gqa_decode_plan, gqa_release.
+  gqa_status_string, gqa_get_device_status, gqa_decode_plan, gqa_release,
+  and the failure-injection hooks gqa_test_set_wait_limit_ns,
+  gqa_test_fail_workspace_allocs.
 """
 from __future__ import annotations
 
@@ -35,7 +37,7 @@ GQA_DEV_BAD_PAGE = 0x10
 EXPORTED = ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host",
             "gqa_status_string", "gqa_get_device_status", "gqa_decode_plan", "gqa_release",
             "gqa_decode_noalloc", "gqa_decode_fp8", "gqa_rope_append", "gqa_decode_paged", "gqa_prefill_chunk",
-            "gqa_meanpool_kv_heads")
+            "gqa_meanpool_kv_heads", "gqa_test_set_wait_limit_ns", "gqa_test_fail_workspace_allocs")
 
 _lib = None
 
@@ -80,6 +82,10 @@ def load_library():
     lib.gqa_decode_plan.restype = i
     lib.gqa_release.argtypes = []
     lib.gqa_release.restype = None
+    lib.gqa_test_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.gqa_test_set_wait_limit_ns.restype = None
+    lib.gqa_test_fail_workspace_allocs.argtypes = [i]
+    lib.gqa_test_fail_workspace_allocs.restype = None
     _lib = lib
     return lib
 
@@ -335,3 +341,14 @@ def gqa_decode_plan(B, Hq, Hkv, D, Lmax):
 
 def gqa_release():
     load_library().gqa_release()
+
+
+def gqa_test_set_wait_limit_ns(ns: int):
+    """Test hook: pipeline waits of later launches give up after ns
+    nanoseconds (0 restores the default 2 s)."""
+    load_library().gqa_test_set_wait_limit_ns(int(ns))
+
+
+def gqa_test_fail_workspace_allocs(n: int):
+    """Test hook: the next n decode-workspace allocations fail as out of memory."""
+    load_library().gqa_test_fail_workspace_allocs(int(n))

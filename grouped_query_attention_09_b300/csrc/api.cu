@@ -6,17 +6,21 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <vector>
 
 #include "../../include/gqa.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace {
 
 thread_local std::string g_cuda_msg;
 std::mutex g_mu;
+std::atomic<unsigned long long> g_wait_limit_ns{0};  // 0: kWaitLimitNs
+std::atomic<int> g_fail_allocs{0};                   // workspace allocations still to fail
 
 struct DeviceCtx {
   bool ready = false;
@@ -37,6 +41,12 @@ std::vector<DeviceCtx> g_dev;
 int cuda_fail(cudaError_t e) {
   g_cuda_msg = std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e);
   return GQA_ERR_CUDA;
+}
+
+// A workspace allocation, or the failure a test asked for.
+cudaError_t ws_malloc(void** p, size_t bytes) {
+  if (gqa::take_injected_alloc_failure()) return cudaErrorMemoryAllocation;
+  return cudaMalloc(p, bytes);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -126,14 +136,16 @@ int decode_locked(DeviceCtx& c, const void* q, const void* k, const void* v, con
       if (c.ws_part) cudaFree(c.ws_part);
       c.ws_part = nullptr;
       c.ws_part_cap = 0;
-      if ((e = cudaMalloc(&c.ws_part, plan.ws_part_floats * sizeof(float))) != cudaSuccess) return cuda_fail(e);
+      if ((e = ws_malloc(reinterpret_cast<void**>(&c.ws_part), plan.ws_part_floats * sizeof(float))) != cudaSuccess)
+        return cuda_fail(e);
       c.ws_part_cap = plan.ws_part_floats;
     }
     if (plan.ws_counters > c.counters_cap) {
       if (c.counters) cudaFree(c.counters);
       c.counters = nullptr;
       c.counters_cap = 0;
-      if ((e = cudaMalloc(&c.counters, plan.ws_counters * sizeof(int))) != cudaSuccess) return cuda_fail(e);
+      if ((e = ws_malloc(reinterpret_cast<void**>(&c.counters), plan.ws_counters * sizeof(int))) != cudaSuccess)
+        return cuda_fail(e);
       if ((e = cudaMemset(c.counters, 0, plan.ws_counters * sizeof(int))) != cudaSuccess) return cuda_fail(e);
       c.counters_cap = plan.ws_counters;
     }
@@ -163,6 +175,18 @@ size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 }  // namespace
 
 namespace gqa {
+
+unsigned long long pipeline_wait_limit_ns() {
+  const unsigned long long v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return v ? v : kWaitLimitNs;
+}
+
+bool take_injected_alloc_failure() {
+  int n = g_fail_allocs.load();
+  while (n > 0)
+    if (g_fail_allocs.compare_exchange_weak(n, n - 1)) return true;
+  return false;
+}
 
 CUresult encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1,
                              uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
@@ -447,6 +471,9 @@ int gqa_get_device_status(void* stream, uint32_t* flags) {
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
   if ((e = cudaMemcpy(&v, c->err, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
   if ((e = cudaMemset(c->err, 0, sizeof v)) != cudaSuccess) return cuda_fail(e);
+  unsigned na = 0;
+  if ((e = gqa::noalloc_take_status(&na)) != cudaSuccess) return cuda_fail(e);
+  v |= na;
   if ((v & GQA_DEV_WAIT_TIMEOUT) && c->counters) {
     // A decode that gave up may have left arrival counters half counted.
     if ((e = cudaMemset(c->counters, 0, c->counters_cap * sizeof(int))) != cudaSuccess) return cuda_fail(e);
@@ -472,6 +499,10 @@ int gqa_decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int* tile_keys, int
   *num_ctas = plan.num_ctas;
   return GQA_OK;
 }
+
+void gqa_test_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store(ns); }
+
+void gqa_test_fail_workspace_allocs(int n) { g_fail_allocs.store(n > 0 ? n : 0); }
 
 void gqa_release(void) {
   std::lock_guard<std::mutex> lk(g_mu);

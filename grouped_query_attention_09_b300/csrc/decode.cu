@@ -79,6 +79,7 @@ struct Params {
   const int32_t* block_table;  // paged cache (else null): [B][max_pages] page of each logical page
   int page_size, max_pages, num_pages;
   int prefetch_tiles;  // > 0: one CTA per (b, kv head) pair; prefetch its first tiles into L2 at launch
+  unsigned long long wait_ns;  // pipeline-wait limit
 };
 
 struct SmemLayout {
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(288, 1)
         const int i = (int)(t - s_c);
         const int s = ig * SG + us;
         if (lap > 0) {
-          if (!mbar_wait_bounded(&empty[s], (uint32_t)((lap - 1) & 1), abort_flag, p.err)) break;
+          if (!mbar_wait_bounded(&empty[s], (uint32_t)((lap - 1) & 1), abort_flag, p.err, p.wait_ns)) break;
         }
         if (++ig == NG) {
           ig = 0;
@@ -463,7 +464,7 @@ __global__ void __launch_bounds__(288, 1)
         us = 0;
         ph ^= 1u;
       }
-      if (live) live = mbar_wait_bounded(&full[s], par, abort_flag, p.err);
+      if (live) live = mbar_wait_bounded(&full[s], par, abort_flag, p.err, p.wait_ns);
       if (live) {
         uint32_t kbase = smem_u32(smem + s * L.stage_bytes);
         uint32_t vbase = kbase + L.k_bytes;
@@ -947,6 +948,7 @@ cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t s
   p.page_size = a.page_size;
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
+  p.wait_ns = pipeline_wait_limit_ns();
   p.prefetch_tiles = 0;
   if (!a.block_table && plan.num_ctas == a.B * a.Hkv)
     p.prefetch_tiles = std::min(plan.stages, (a.Lmax + kBN - 1) / kBN);

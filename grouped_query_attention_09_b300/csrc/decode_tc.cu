@@ -73,6 +73,7 @@ struct TcParams {
   float scale_log2;
   const int32_t* block_table;  // paged cache (else null): [B][max_pages]
   int page_size, max_pages, num_pages;
+  unsigned long long wait_ns;  // pipeline-wait limit
 };
 
 struct TcLayout {
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           kvy -= lp * p.page_size;
         }
         if (t == s_c || it.lt == 0) {
-          ok = mbar_wait_bounded(q_empty, (seg & 1) ^ 1, abort_flag, p.err);
+          ok = mbar_wait_bounded(q_empty, (seg & 1) ^ 1, abort_flag, p.err, p.wait_ns);
           if (!ok) break;
           mbar_arrive_expect_tx(q_full, kQBytes);
           tma_load_3d(q_tile, &tmQ, 0, 0, z, q_full, pol);
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = kv ? vslot(i) : kslot(i);
           const uint32_t par = kv ? vpar(i) : kpar(i);
           if (2 * i + kv >= p.stages) {
-            ok = mbar_wait_bounded(&kv_empty[s], par ^ 1, abort_flag, p.err);
+            ok = mbar_wait_bounded(&kv_empty[s], par ^ 1, abort_flag, p.err, p.wait_ns);
             if (!ok) break;
           }
           uint8_t* dst = ring + s * kBlockBytes;
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dk = tc::sdesc_sw128(smem_u32(ring), 16, 1024);
     const uint64_t dv = tc::sdesc_sw128(smem_u32(ring), kHalf, 1024);
     auto wait = [&](uint64_t* bar, uint32_t parity) {
-      const bool w = mbar_wait_bounded(bar, parity, abort_flag, p.err);
+      const bool w = mbar_wait_bounded(bar, parity, abort_flag, p.err, p.wait_ns);
       return __all_sync(0xffffffffu, w);
     };
     auto commit = [&](uint64_t* bar) {
@@ -423,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int valid = min(kBN, len_b - it.lt * kBN);  // keys of this block that exist (>= 1)
       {
-        const bool w = mbar_wait_bounded(&s_full[i & 1], (uint32_t)((i >> 1) & 1), abort_flag, p.err);
+        const bool w = mbar_wait_bounded(&s_full[i & 1], (uint32_t)((i >> 1) & 1), abort_flag, p.err, p.wait_ns);
         ok = __all_sync(0xffffffffu, w) && ok;
       }
       tc::fence_after_sync();
@@ -480,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
         if (any_rebase && !first) {
           // O holds blocks up to i - 1: wait for that P V, then re-base it.
-          const bool w = mbar_wait_bounded(o_done, (uint32_t)((i - 1) & 1), abort_flag, p.err);
+          const bool w = mbar_wait_bounded(o_done, (uint32_t)((i - 1) & 1), abort_flag, p.err, p.wait_ns);
           if (__all_sync(0xffffffffu, w)) {
             tc::fence_after_sync();
 #pragma unroll 1
@@ -500,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Cache rows at and past seqlens[b] may hold anything (NaN included):
         // zero them in the V block so that P = 0 there contributes exactly 0.
         uint8_t* vb = ring + vslot(i) * kBlockBytes;
-        const bool w = mbar_wait_bounded(&kv_full[vslot(i)], vpar(i), abort_flag, p.err);
+        const bool w = mbar_wait_bounded(&kv_full[vslot(i)], vpar(i), abort_flag, p.err, p.wait_ns);
         ok = __all_sync(0xffffffffu, w) && ok;
         if (ok) {
           const int nchunks = (kBN - valid) * 16;  // 16-byte chunks over both halves
@@ -517,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (last) {
         // ---- end of a piece: O / l to the output, or a partial for the merge
         {
-          const bool w = mbar_wait_bounded(o_full, (uint32_t)(seg & 1), abort_flag, p.err);
+          const bool w = mbar_wait_bounded(o_full, (uint32_t)(seg & 1), abort_flag, p.err, p.wait_ns);
           ok = __all_sync(0xffffffffu, w) && ok;
         }
         ++seg;
@@ -763,6 +764,7 @@ cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaSt
   p.page_size = a.page_size;
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
+  p.wait_ns = pipeline_wait_limit_ns();
   static std::atomic<unsigned long long> attr_set{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -8,6 +8,19 @@
 
 namespace gqa {
 
+// Limit of the kernels' pipeline waits for launches made now (nanoseconds):
+// kWaitLimitNs unless gqa_test_set_wait_limit_ns chose another.
+unsigned long long pipeline_wait_limit_ns();
+
+// Test hook of gqa_test_fail_workspace_allocs: true if this workspace
+// allocation is to fail (consumes one of the requested failures).
+bool take_injected_alloc_failure();
+
+// Reads and clears the status word of gqa_decode_noalloc's fixed scratch on
+// the current device (0 if that entry point was never set up there).
+// Synchronous; allocates nothing.
+cudaError_t noalloc_take_status(unsigned* flags);
+
 // Encodes a 3-D bf16 tiled tensor map (dims innermost first, strides in bytes
 // for dims 1 and 2) with 128-byte swizzle and zero fill outside the tensor.
 CUresult encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1,

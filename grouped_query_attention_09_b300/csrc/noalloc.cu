@@ -28,8 +28,11 @@ constexpr size_t kMaxPartFloats = GQA_NOALLOC_MAX_PART_FLOATS;
 constexpr size_t kCountersOff = 256;
 constexpr size_t kPartOff = (kCountersOff + 4 * (kMaxPairs + 2) + 255) / 256 * 256;
 constexpr size_t kScratchBytes = kPartOff + 4 * kMaxPartFloats;
+static_assert(kScratchBytes == GQA_NOALLOC_SCRATCH_BYTES, "gqa.h states the scratch size callers plan for");
 
-// Every GPU that loads the library holds this array until the process exits.
+// Every GPU on which this array's module is loaded (at the first
+// gqa_decode_noalloc call there, see scratch_for_current_device) holds it
+// until the process exits.
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -38,7 +41,11 @@ void* g_na_ptr[kMaxDevices];  // device address of g_decode_scratch, per device
 int g_na_sms[kMaxDevices];
 
 // Once per device, with that device current: resolve the array's device
-// address (in host code the symbol is only a host-side stand-in).
+// address (in host code the symbol is only a host-side stand-in).  With the
+// CUDA runtime's lazy module loading (the default) this lookup is also what
+// loads the module holding the array, and so what commits its
+// GQA_NOALLOC_SCRATCH_BYTES of device memory on this device: the first call
+// on a device belongs at start-up.
 int scratch_for_current_device(void** ptr, int* sms) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -71,6 +78,31 @@ int scratch_for_current_device(void** ptr, int* sms) {
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+namespace gqa {
+
+cudaError_t noalloc_take_status(unsigned* flags) {
+  *flags = 0;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_na_mu);
+    p = g_na_ptr[dev];
+  }
+  if (!p) return cudaSuccess;
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return e;
+  if (v && (e = cudaMemset(p, 0, sizeof v)) != cudaSuccess) return e;
+  *flags = v;
+  return cudaSuccess;
+}
+
+}  // namespace gqa
 
 extern "C" int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                   const int32_t* seqlens, void* out, int B, int Hq, int Hkv, int D,

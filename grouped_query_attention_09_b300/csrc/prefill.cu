@@ -19,23 +19,29 @@
 // Warp roles (320 threads, one CTA per SM):
 //   warps 0-3  softmax of query tile 0 (thread = one query row = one TMEM lane)
 //   warps 4-7  softmax of query tile 1
-//   warp  8    TMA producer: Q tiles, then K/V blocks into a 3-stage ring
-//   warp  9    TMEM owner and tcgen05.mma issuer (one thread)
+//   warp  8    TMA producer: the two Q tiles of a unit, then K/V blocks into a
+//              5-stage ring of 32 KiB slots (a slot holds one K or one V block)
+//   warp  9    TMEM owner and tcgen05.mma issuer (the whole warp walks the
+//              schedule, one elected lane issues)
 //
 // Per KV block j of a unit:
-//   S_t = Q_t K_j^T           tcgen05.mma, A = Q_t (smem), B = K_j (smem, K-major),
-//                             fp32 accumulator in TMEM columns [128t, 128t+128)
+//   S_t = Q_t K_j^T           SS MMA: A = Q_t (smem, K-major), B = K_j (smem,
+//                             K-major), fp32 accumulator in TMEM columns
+//                             [128t, 128t + 128)
 //   softmax_t                 thread r loads row r of S_t from TMEM, masks the
 //                             diagonal block, keeps a running max (re-based only
 //                             when it grows by more than 2^8 in log2 units, so O
-//                             is rescaled rarely) and the running sum, writes
-//                             P = exp2(S*scale*log2e - m) as bf16 into smem
-//   O_t += P_t V_j            tcgen05.mma, A = P_t (smem), B = V_j (smem, MN-major),
-//                             fp32 accumulator in TMEM columns [256+128t, ...)
-// The MMA thread interleaves the two tiles (S0, S1, PV0, S0', PV1, S1', ...),
-// so that the tensor pipe works on one tile while the other tile's softmax runs.
-// At the end of a unit each softmax thread reads its O row, divides by the
-// running sum and stores bf16 to global memory.
+//                             is rescaled rarely) and the running sum, and writes
+//                             P = exp2(S*scale*log2e - m) as bf16 pairs back into
+//                             the first 64 TMEM columns of S_t
+//   O_t += P_t V_j            TS MMA: A = P_t read from TMEM, B = V_j (smem,
+//                             MN-major), fp32 accumulator in TMEM columns
+//                             [256 + 128t, 256 + 128t + 128)
+// The MMA warp interleaves the two tiles (S0, S1, PV0, S0', PV1, S1', ...),
+// so that the tensor pipe works on one tile while the other tile's softmax
+// runs.  TMEM: S0, S1, O0, O1 = 512 columns.  At the end of a unit each
+// softmax thread reads its O row, divides by the running sum and stores bf16
+// to global memory.
 //
 // Every wait is bounded; on expiry the kernel flags GQA_DEV_WAIT_TIMEOUT,
 // every role leaves its loop, in-flight copies and MMAs are waited for (again
@@ -83,6 +89,7 @@ struct Params {
   int units;
   float scale_log2;  // (1 / sqrt(D)) * log2(e)
   unsigned* err;
+  unsigned long long wait_ns;  // pipeline-wait limit
 };
 
 struct Unit {
@@ -185,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = my_unit(p, 0); u >= 0 && ok; u = my_unit(p, ++i)) {
         const Unit x = unit_at(p, u);
         for (int t = 0; t < 1 + p.two && ok; ++t) {
-          ok = mbar_wait_bounded(&q_empty[t], (i & 1) ^ 1, abort_flag, p.err);
+          ok = mbar_wait_bounded(&q_empty[t], (i & 1) ^ 1, abort_flag, p.err, p.wait_ns);
           if (!ok) break;
           uint8_t* dst = smem + kOffQ + t * kTileBytes;
           mbar_arrive_expect_tx(&q_full[t], kTileBytes);
@@ -199,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kv = 0; kv < 2; ++kv) {
             const int s = kv_it % kStages;
             const uint32_t par = (kv_it / kStages) & 1;
-            ok = mbar_wait_bounded(&kv_empty[s], par ^ 1, abort_flag, p.err);
+            ok = mbar_wait_bounded(&kv_empty[s], par ^ 1, abort_flag, p.err, p.wait_ns);
             if (!ok) break;
             uint8_t* dst = smem + kOffRing + s * kTileBytes;
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
@@ -257,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) tc::commit(bar);
     };
     auto wait = [&](uint64_t* bar, uint32_t parity) {
-      const bool w = mbar_wait_bounded(bar, parity, abort_flag, p.err);
+      const bool w = mbar_wait_bounded(bar, parity, abort_flag, p.err, p.wait_ns);
       return __all_sync(0xffffffffu, w);
     };
     uint32_t kv_it = 0, pc0 = 0, pc1 = 0;
@@ -345,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qi = x.qb * kBM + r;  // query position of this row
       float m_use = -INFINITY, l = 0.f;
       for (int jb = 0; jb < x.n; ++jb) {
-        ok = mbar_wait_bounded(&s_full[t], sc & 1, abort_flag, p.err);
+        ok = mbar_wait_bounded(&s_full[t], sc & 1, abort_flag, p.err, p.wait_ns);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ++sc;
@@ -430,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&p_full[t]);
       }
       if (!ok) break;
-      ok = mbar_wait_bounded(&o_full[t], oc & 1, abort_flag, p.err);
+      ok = mbar_wait_bounded(&o_full[t], oc & 1, abort_flag, p.err, p.wait_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ++oc;
@@ -499,6 +506,7 @@ cudaError_t prefill_launch(const PrefillArgs& a, int sm_count, cudaStream_t stre
   p.units = (int)units;
   p.scale_log2 = (1.0f / sqrtf((float)a.D)) * 1.4426950408889634f;
   p.err = a.err;
+  p.wait_ns = pipeline_wait_limit_ns();
   static std::atomic<unsigned long long> attr_set{0};  // one bit per device ordinal < 64
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

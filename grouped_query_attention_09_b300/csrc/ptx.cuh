@@ -14,7 +14,10 @@
 namespace gqa {
 
 // How long a pipeline wait may spin before it gives up and flags
-// GQA_DEV_WAIT_TIMEOUT (nanoseconds of %globaltimer).
+// GQA_DEV_WAIT_TIMEOUT (nanoseconds of %globaltimer).  Kernels take their
+// pipeline-wait limit as a launch parameter (this value unless a test sets a
+// shorter one); the waits that drain in-flight copies and MMAs before a CTA
+// exits always use this value.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -64,17 +67,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase of `bar` with the given parity has completed.
-// Gives up after kWaitLimitNs, or as soon as *abort (shared) is non-zero:
-// then it records GQA_DEV_WAIT_TIMEOUT in *err, raises *abort and returns false.
+// Gives up after limit_ns, or as soon as *abort (shared) is non-zero: on
+// expiry it records GQA_DEV_WAIT_TIMEOUT in *err, raises *abort and returns
+// false; after another thread's expiry it returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort, unsigned* err) {
+                                                  volatile int* abort, unsigned* err,
+                                                  unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
+  for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         atomicOr(err, GQA_DEV_WAIT_TIMEOUT);
         *abort = 1;
         return false;

@@ -274,25 +274,32 @@ GQA_API int gqa_prefill_host(const void* q_host, const void* k_host, const void*
  *
  * Arguments, layouts, results and device-side fallbacks are those of
  * gqa_decode.  Differences:
- *   - the split workspace is a fixed device array inside libgqa.so
- *     (GQA_NOALLOC_SCRATCH_BYTES, held by every GPU that loads the library
- *     until the process exits); the call makes no cudaMalloc / cudaFree and
+ *   - the split workspace is a fixed device array inside libgqa.so of
+ *     GQA_NOALLOC_SCRATCH_BYTES; the call makes no cudaMalloc / cudaFree and
  *     calls no allocating routine;
- *   - sizes whose workspace exceeds it return GQA_ERR_TOO_LARGE: at most
- *     GQA_NOALLOC_MAX_PAIRS (b, kv head) pairs (B * Hkv) and
- *     GQA_NOALLOC_MAX_PART_FLOATS partial floats (one CTA per SM x 2 x G x
- *     (D + 2)); every workload with G <= 32, D = 128 and B * Hkv <= 8192 fits;
- *   - the first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture;
+ *   - the first call on a device sets the array up there, with that device
+ *     current: it looks up the array's device address, and with the CUDA
+ *     runtime's default lazy module loading that lookup loads the module
+ *     holding the array, which commits GQA_NOALLOC_SCRATCH_BYTES of device
+ *     memory on that device until the process exits.  Make that first call at
+ *     start-up, before a memory pool reserves the free HBM and before any
+ *     stream capture; later calls change no device-memory total;
+ *   - sizes whose workspace exceeds the array return GQA_ERR_TOO_LARGE: at
+ *     most GQA_NOALLOC_MAX_PAIRS (b, kv head) pairs (B * Hkv) and
+ *     GQA_NOALLOC_MAX_PART_FLOATS partial floats (persistent CTAs x 2 x G x
+ *     (D + 2), the CTAs at most 160); every workload with G <= 32, D = 128 and
+ *     B * Hkv <= 8192 fits;
  *   - every call, on every stream, shares the one array: calls that overlap
  *     on the GPU race and give wrong results -- order them (one stream, or
  *     events).  Each call clears the parts that must start at zero;
- *   - the device status bits of this call are kept in the array and are not
- *     reported by gqa_get_device_status.
+ *   - the device status bits of these calls are kept in the array and are
+ *     reported (and cleared) by gqa_get_device_status together with the
+ *     library's own word; that read allocates nothing.
  */
 #define GQA_NOALLOC_MAX_PAIRS 8192
-#define GQA_NOALLOC_MAX_PART_FLOATS 1310720
-#define GQA_NOALLOC_SCRATCH_BYTES (256 + 4 * (GQA_NOALLOC_MAX_PAIRS + 2) + 4 * GQA_NOALLOC_MAX_PART_FLOATS)
+#define GQA_NOALLOC_MAX_PART_FLOATS 1331200
+#define GQA_NOALLOC_SCRATCH_BYTES \
+  ((256 + 4 * (GQA_NOALLOC_MAX_PAIRS + 2) + 255) / 256 * 256 + 4 * GQA_NOALLOC_MAX_PART_FLOATS)
 GQA_API int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* seqlens, void* out, int B, int Hq, int Hkv, int D,
                                int Lmax, float scale, void* stream);
@@ -302,13 +309,38 @@ GQA_API int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v
 GQA_API const char* gqa_status_string(int status);
 
 /* Synchronises `stream`, then reads and clears the current device's status
- * word (GQA_DEV_* bits) into *flags.  Returns GQA_OK or GQA_ERR_CUDA. */
+ * word (GQA_DEV_* bits) into *flags -- the OR of the word every entry point
+ * but gqa_decode_noalloc writes and, once gqa_decode_noalloc has run on the
+ * device, the word in its fixed scratch.  After GQA_DEV_WAIT_TIMEOUT it also
+ * zeroes the decode workspace's arrival counters.  Returns GQA_OK or
+ * GQA_ERR_CUDA.  (The status comes back through a pointer, not as the return
+ * value, so that a failure to read it is told apart from the bits.) */
 GQA_API int gqa_get_device_status(void* stream, uint32_t* flags);
 
 /* Number of key tiles of the decode split and persistent CTAs the next
  * gqa_decode with these sizes would use, for tests and tuning:
  * *tile_keys, *num_ctas.  Returns GQA_OK or an argument error. */
 GQA_API int gqa_decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int* tile_keys, int* num_ctas);
+
+/*
+ * Test hooks: failure injection for the error paths (the paper pages have
+ * no counterpart).  Not for production use.
+ *
+ * gqa_test_set_wait_limit_ns -- every pipeline wait (a producer waiting for a
+ * free ring slot, a consumer for its data, the MMA issuer for the softmax)
+ * of kernels launched after this call gives up after `ns` nanoseconds
+ * instead of the default 2 s; 0 restores the default.  A wait that gives up
+ * sets GQA_DEV_WAIT_TIMEOUT and the kernel returns early with its output
+ * invalid; nothing traps.  The waits with which a CTA lets its own copies and
+ * MMAs land before it exits keep the 2 s limit.
+ *
+ * gqa_test_fail_workspace_allocs -- the next `n` allocations of the decode
+ * workspace (made when a decode needs a larger one) fail as out of memory
+ * without calling cudaMalloc, so the call returns GQA_ERR_CUDA; n <= 0
+ * cancels.
+ */
+GQA_API void gqa_test_set_wait_limit_ns(unsigned long long ns);
+GQA_API void gqa_test_fail_workspace_allocs(int n);
 
 /* Frees every device buffer the library holds on every device it touched.
  * No call may be in flight.  Safe to call more than once. */

@@ -11,7 +11,11 @@ plausible slip in the oracle fails at least one of them:
 * a causal diagonal off by one / a mask that leaks the future: row 0 = v_0,
   the i/2 staircase, future-perturbation invariance;
 * reading cache rows past seqlens[b]: the NaN-tail test;
-* a lossy bf16 widening: exact bit patterns.
+* a lossy bf16 widening: exact bit patterns;
+* a rotary embedding with the wrong pairing ((2i, 2i + 1) instead of
+  (i, i + D/2)) or the wrong rate (base^(-i/D)): the basis-vector closed form
+  and an independent numpy rotate-half statement (both slips are planted and
+  shown to fail).
 """
 import math
 
@@ -413,6 +417,118 @@ def test_rope_scores_depend_only_on_relative_position(oracle_mod):
     np.testing.assert_allclose(vals, vals[0], rtol=1e-9)
     other = float((_rope(oracle_mod, q, [11]) @ _rope(oracle_mod, k, [3]).T)[0, 0])
     assert abs(other - vals[0]) > 1e-6
+
+
+# The next pins fix the two conventions the pages leave open (the GQA paper
+# notes, "QA 相关", call apply_rotary_pos_emb without defining it; the reading
+# taken is the Llama "rotate half" form): WHICH coordinates form a rotated pair
+# -- (i, i + D/2), not (2i, 2i + 1) -- and the angular rate of pair i,
+# base^(-2i/D), not base^(-i/D).  The identity / norm / composition /
+# relative-position pins above hold for any pairing and any rate, so they
+# cannot tell these apart.  Each check below is written as a function of the
+# rotation under test, and the last test plants both plausible slips (as
+# numpy stand-ins for a mistaken oracle) to show that each one fails.
+
+def _theta(D, base):
+    return base ** (-2.0 * np.arange(D // 2) / D)
+
+
+def _basis_closed_form_errors(rope, D, base, positions):
+    """Largest deviation of rope(e_j, p) from the rotate-half closed form over
+    every basis vector e_j and the given positions: for i < D/2,
+      e_i        -> cos(p t_i) e_i + sin(p t_i) e_{i+D/2}
+      e_{i+D/2}  -> -sin(p t_i) e_i + cos(p t_i) e_{i+D/2},   t_i = base^(-2i/D)."""
+    h = D // 2
+    eye = np.eye(D)
+    worst = 0.0
+    for p in positions:
+        y = rope(eye, [p] * D, base)  # row j = image of e_j
+        ang = p * _theta(D, base)
+        want = np.zeros((D, D))
+        idx = np.arange(h)
+        want[idx, idx] = np.cos(ang)
+        want[idx, idx + h] = np.sin(ang)
+        want[idx + h, idx] = -np.sin(ang)
+        want[idx + h, idx + h] = np.cos(ang)
+        worst = max(worst, float(np.abs(y - want).max()))
+    return worst
+
+
+def _numpy_rotate_half(x, pos, base):
+    """The Llama statement, written independently of the oracle: a table of
+    angles pos x inv_freq by np.outer, duplicated over both halves, then
+    x * cos + rotate_half(x) * sin with rotate_half(x) = [-x2, x1]."""
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    inv_freq = 1.0 / (base ** (np.arange(0, D, 2, dtype=np.float64) / D))
+    ang = np.outer(np.asarray(pos, dtype=np.float64), inv_freq)
+    emb = np.concatenate([ang, ang], axis=-1)
+    x1, x2 = x[..., : D // 2], x[..., D // 2:]
+    rot = np.concatenate([-x2, x1], axis=-1)
+    return x * np.cos(emb) + rot * np.sin(emb)
+
+
+def _oracle_rope(oracle_mod):
+    return lambda x, pos, base: _rope(oracle_mod, np.asarray(x, dtype=np.float64), pos, base)
+
+
+_CONV_CASES = [(8, 10000.0, [1, 3, 77]), (16, 500.0, [2, 1000]), (64, 10000.0, [1, 4095]),
+               (128, 10000.0, [1, 5, 16000]), (128, 1e6, [7, 131071])]
+
+
+@pytest.mark.parametrize("D,base,positions", _CONV_CASES)
+def test_rope_basis_vectors_closed_form(oracle_mod, D, base, positions):
+    """Pins the pairing (i, i + D/2) and the rate base^(-2i/D) exactly: the
+    image of every basis vector is one cos/sin pair at a known place (the
+    bound allows the rounding of angles up to ~1.3e5 rad)."""
+    assert _basis_closed_form_errors(_oracle_rope(oracle_mod), D, base, positions) < 1e-10
+
+
+@pytest.mark.parametrize("D,base", [(16, 10000.0), (128, 10000.0), (128, 500000.0), (256, 10000.0)])
+def test_rope_matches_numpy_rotate_half(oracle_mod, D, base):
+    rng = np.random.default_rng(D)
+    x = rng.standard_normal((9, D))
+    pos = rng.integers(0, 20000, 9)
+    np.testing.assert_allclose(_rope(oracle_mod, x, pos, base), _numpy_rotate_half(x, pos, base),
+                               rtol=0, atol=1e-10)
+
+
+def _mistaken_adjacent_pairs(x, pos, base):
+    """Slip 1: GPT-J style pairs (2i, 2i + 1) at rate base^(-2i/D)."""
+    x = np.asarray(x, dtype=np.float64).copy()
+    D = x.shape[-1]
+    ang = np.outer(np.asarray(pos, dtype=np.float64), _theta(D, base))
+    a, b = x[..., 0::2].copy(), x[..., 1::2].copy()
+    x[..., 0::2] = a * np.cos(ang) - b * np.sin(ang)
+    x[..., 1::2] = b * np.cos(ang) + a * np.sin(ang)
+    return x
+
+
+def _mistaken_rate(x, pos, base):
+    """Slip 2: rotate-half pairs at rate base^(-i/D)."""
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    ang = np.outer(np.asarray(pos, dtype=np.float64), base ** (-np.arange(D // 2) / D))
+    x1, x2 = x[..., : D // 2], x[..., D // 2:]
+    return np.concatenate([x1 * np.cos(ang) - x2 * np.sin(ang), x2 * np.cos(ang) + x1 * np.sin(ang)], axis=-1)
+
+
+@pytest.mark.parametrize("mistake", [_mistaken_adjacent_pairs, _mistaken_rate])
+def test_rope_convention_pins_catch_planted_slips(oracle_mod, mistake):
+    """Each plausible slip passes the convention-blind pins (identity at p = 0,
+    pair norms up to its own pairing, composition) yet fails both pins above."""
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((4, 32))
+    assert np.array_equal(mistake(x, [0] * 4, 10000.0), x)  # it is a rotation too
+    a, b = rng.integers(0, 500, 4), rng.integers(0, 500, 4)
+    np.testing.assert_allclose(mistake(mistake(x, a, 10000.0), b, 10000.0), mistake(x, a + b, 10000.0),
+                               rtol=1e-9, atol=1e-9)
+    for D, base, positions in _CONV_CASES:
+        assert _basis_closed_form_errors(mistake, D, base, positions) > 1e-3
+    pos = rng.integers(1, 20000, 4)
+    assert np.abs(mistake(x, pos, 10000.0) - _numpy_rotate_half(x, pos, 10000.0)).max() > 1e-3
+    # and the oracle itself is not one of them
+    assert _basis_closed_form_errors(_oracle_rope(oracle_mod), 32, 10000.0, [3]) < 1e-12
 
 
 def test_rope_append_rows_and_full_cache(oracle_mod):

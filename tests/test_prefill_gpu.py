@@ -6,9 +6,8 @@ query tiles and 128-key blocks, ragged tails, both causal settings, even G
 (two query heads share each K/V block) and odd G (one head per unit), the MHA
 and MQA endpoints, and grids where every CTA walks several units.  The
 full-size causal workload (B=4, L=2048, Hq=32, Hkv=8, D=128) is checked on
-sampled rows, in the launch configuration the benchmark times.
+every element, in the launch configuration the benchmark times.
 """
-import numpy as np
 import pytest
 import torch
 
@@ -61,29 +60,17 @@ def test_peaky_softmax_rebases_running_max(gqa_lib, oracle_mod, cuda_device):
         assert_parity(out.double().numpy(), oracle_prefill(oracle_mod, q, k, v, causal), f"peaky causal={causal}")
 
 
-def _sample_rows(w, rng, n_random=48):
-    heads = sorted({0, 1, 2, 3, w.G if hasattr(w, "G") else 4, w.Hq // 2 + 1, w.Hq - 1})
-    fixed = [0, 1, 2, 63, 127, 128, 129, 255, 1023, 1024, w.L - 129, w.L - 128, w.L - 2, w.L - 1]
-    rows = []
-    for b in range(w.B):
-        for h in heads:
-            idx = set(i for i in fixed if 0 <= i < w.L) | set(rng.integers(0, w.L, n_random).tolist())
-            rows += [(b, h, i) for i in sorted(idx)]
-    return np.array(rows, dtype=np.int32)
-
-
-def test_full_size_causal_workload_sampled_rows(gqa_lib, oracle_mod, cuda_device):
-    """The benchmark's prefill workload at full size; rows sampled across every
-    batch, first/middle/last heads of several groups, tile edges and the end."""
+def test_full_size_causal_workload_every_element(gqa_lib, oracle_mod, cuda_device):
+    """The benchmark's prefill workload at full size (B=4, L=2048, Hq=32,
+    Hkv=8, D=128, causal), in the launch configuration the benchmark times:
+    every element of the output against the oracle (about 137 GFLOP of fp64
+    on the host cores, a few seconds with OpenMP)."""
     w = W.WORKLOADS["prefill"]
     q, k, v = W.make_prefill_inputs(w)
     out, flags = run_prefill(gqa_lib, q, k, v, w.causal, cuda_device)
     assert flags == 0
-    rows = _sample_rows(w, np.random.default_rng(5))
-    ref = oracle_prefill(oracle_mod, q, k, v, w.causal, rows=rows)
-    got = out[rows[:, 0], rows[:, 1], rows[:, 2]].double().numpy()
-    assert_parity(got, ref, "prefill full size")
-    assert torch.isfinite(out.float()).all()
+    ref = oracle_prefill(oracle_mod, q, k, v, w.causal)
+    assert_parity(out.double().numpy(), ref, "prefill full size")
 
 
 def test_repeatable_side_stream_and_host_entry(gqa_lib, cuda_device):

@@ -3,22 +3,21 @@
 It serves callers that cannot let the library allocate device memory (a
 serving engine that owns all HBM through its own pool; a latency-critical
 loop that may not call cudaMalloc after start-up).  Its workspace is a fixed
-array inside libgqa.so.  These tests call it through the C ABI and check it
-against gqa_decode, on two calls in a row, with the tolerance of the decode
-parity tests.  The file is named so that pytest collects it last.
+array inside libgqa.so.  These tests call it through the C ABI, two calls in
+a row, and check each call against gqa_decode and against the fp64 oracle with
+the tolerance of the decode parity tests; they also check that once the first
+call has set the array up, later calls change no device-memory total.  The
+file is named so that pytest collects it last.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 from grouped_query_attention_09_b300 import workloads as W
+from parity import ATOL, RTOL, assert_parity
 
 pytestmark = pytest.mark.gpu
-
-ATOL = 1e-2
-RTOL = 1e-2
 
 
 def _ptr(t):
@@ -32,22 +31,35 @@ def call_noalloc(lib, q, k, v, sl, out, scale, stream):
                                   ctypes.c_float(scale), ctypes.c_void_p(stream.cuda_stream))
 
 
-@pytest.mark.parametrize("name", ["mqa", "llama3_8b"])
-def test_noalloc_matches_gqa_decode_twice(gqa_lib, cuda_device, name):
+def _oracle(oracle_mod, q, k, v, sl, scale):
+    return oracle_mod.decode(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), sl.numpy(), scale)
+
+
+@pytest.mark.parametrize("name", ["mqa", "llama3_8b", "llama2_70b"])
+def test_noalloc_matches_gqa_decode_twice(gqa_lib, oracle_mod, cuda_device, name):
     lib = gqa_lib.load_library()
     w = W.WORKLOADS[name]
-    q, k, v, sl = [t.to(cuda_device) for t in W.make_decode_inputs(w)]
+    q, k, v, sl = W.make_decode_inputs(w)
+    qd, kd, vd, sld = (t.to(cuda_device) for t in (q, k, v, sl))
     stream = torch.cuda.current_stream(cuda_device)
-    ref = gqa_lib.gqa_decode(q, k, v, sl, scale=w.scale).double()
+    ref = gqa_lib.gqa_decode(qd, kd, vd, sld, scale=w.scale).double()
+    exact = _oracle(oracle_mod, q, k, v, sl, w.scale)
+    outs = [torch.full_like(qd, float("nan")) for _ in range(2)]
+    torch.cuda.synchronize()
+    free = []
     for call in range(2):
-        out = torch.full_like(q, float("nan"))
-        st = call_noalloc(lib, q, k, v, sl, out, w.scale, stream)
+        st = call_noalloc(lib, qd, kd, vd, sld, outs[call], w.scale, stream)
         assert st == 0, gqa_lib.gqa_status_string(st)
         torch.cuda.synchronize()
-        got = out.double()
+        free.append(torch.cuda.mem_get_info(cuda_device)[0])
+        got = outs[call].double()
         assert torch.isfinite(got).all(), f"call {call}: non-finite output"
         bad = (got - ref).abs() > ATOL + RTOL * ref.abs()
         assert not bad.any(), f"call {call}: {int(bad.sum())} elements differ from gqa_decode"
+        assert_parity(got.cpu().numpy(), exact, f"{name} no-alloc call {call}")
+    # the first call on this device set the array up; the second allocated nothing
+    assert free[1] == free[0]
+    assert gqa_lib.gqa_get_device_status() == 0
 
 
 def test_noalloc_second_call_with_other_lengths(gqa_lib, oracle_mod, cuda_device):
@@ -65,6 +77,24 @@ def test_noalloc_second_call_with_other_lengths(gqa_lib, oracle_mod, cuda_device
         torch.cuda.synchronize()
         diff = (out.double() - ref.double()).abs()
         assert (diff <= ATOL + RTOL * ref.double().abs()).all()
+        assert_parity(out.double().cpu().numpy(), _oracle(oracle_mod, q, k, v, sl, w.scale), w.name)
+
+
+def test_noalloc_device_status_is_reported(gqa_lib, cuda_device):
+    """The call keeps its status word in the fixed array; gqa_get_device_status
+    reports (and clears) it: a length above the cache capacity is clamped and
+    flagged."""
+    lib = gqa_lib.load_library()
+    stream = torch.cuda.current_stream(cuda_device)
+    w = W.DecodeWorkload("clamp", 2, 8, 2, 128, 256, 256, 256, 8)
+    q, k, v, _ = W.make_decode_inputs(w)
+    sl = torch.tensor([300, 10], dtype=torch.int32)
+    qd, kd, vd, sld = q.to(cuda_device), k.to(cuda_device), v.to(cuda_device), sl.to(cuda_device)
+    out = torch.empty_like(qd)
+    assert gqa_lib.gqa_get_device_status() == 0
+    assert call_noalloc(lib, qd, kd, vd, sld, out, w.scale, stream) == 0
+    assert gqa_lib.gqa_get_device_status() == gqa_lib.GQA_DEV_SEQLEN_CLAMPED
+    assert gqa_lib.gqa_get_device_status() == 0
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(gqa_lib, cuda_device):
