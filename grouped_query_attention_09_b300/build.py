@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libgqa.so")
 SOURCES = ["api.cu", "decode.cu", "decode_tc.cu", "prefill.cu", "rope.cu", "noalloc.cu", "convert.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "tcgen05.cuh"]
+HEADERS = ["ptx.cuh", "internal.h", "tcgen05.cuh", "decode_tc_common.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -45,21 +45,16 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "decode_tc_common.cuh"
 #include "tcgen05.cuh"
 
 namespace gqa {
 namespace {
 
-constexpr int kD = 128;
-constexpr int kBN = 128;                      // keys per block
-constexpr int kBlockBytes = kBN * kD * 2;     // one K or V block: 32 KiB
-constexpr int kHalf = kBlockBytes / 2;        // one 64-column half (128-byte rows)
+using namespace tcd;
+
 constexpr int kQBytes = 128 * kD * 2;         // Q tile: 32 KiB
 constexpr int kThreads = 256;
-constexpr int kMaxBatch = 1024;
-constexpr int kMaxCtasTc = 160;
-constexpr int kSmemLimitTc = 232448;
-constexpr float kRebase = 8.0f;
 constexpr int kColO = 256;
 
 struct TcParams {
@@ -91,46 +86,6 @@ __host__ __device__ inline TcLayout tc_layout(int stages) {
   return l;
 }
 
-struct Iter {
-  int b, j, lt, nb;
-};
-
-__device__ inline void it_seek(Iter& it, long long t, const int* pre, int B, int Hkv) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((long long)Hkv * pre[mid] <= t) lo = mid; else hi = mid - 1;
-  }
-  it.b = lo;
-  it.nb = pre[lo + 1] - pre[lo];
-  const long long r = t - (long long)Hkv * pre[lo];
-  it.j = (int)(r / it.nb);
-  it.lt = (int)(r % it.nb);
-}
-
-__device__ inline void it_next(Iter& it, const int* pre, int B, int Hkv) {
-  if (++it.lt < it.nb) return;
-  it.lt = 0;
-  if (++it.j < Hkv) return;
-  it.j = 0;
-  do { ++it.b; } while (it.b < B && pre[it.b + 1] == pre[it.b]);
-  it.nb = it.b < B ? pre[it.b + 1] - pre[it.b] : 0;
-}
-
-__device__ inline int owner_cta(long long t, long long T, int P) { return (int)(((t + 1) * P + T - 1) / T) - 1; }
-
-__device__ inline int clamp_seq(int len, int Lmax) { return len < 0 ? 0 : (len > Lmax ? Lmax : len); }
-
-__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity, unsigned* err) {
-  const unsigned long long t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(err, GQA_DEV_WAIT_TIMEOUT);
-      return;
-    }
-  }
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const TcParams p) {
@@ -160,6 +115,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.B, Hkv = p.Hkv, G = p.G;
 
+  // The sequence lengths first: their cold read overlaps the set-up below.
+  constexpr int kLensPerThread = kMaxBatch / kThreads;
+  const int per = (B + kThreads - 1) / kThreads;
+  const int lo = tid * per, hi = min(B, lo + per);
+  int lens[kLensPerThread];
+#pragma unroll
+  for (int k = 0; k < kLensPerThread; ++k) lens[k] = (lo + k < hi) ? __ldg(p.seqlens + lo + k) : 0;
+
   if (tid == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
@@ -184,15 +147,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- blocks per sequence and their exclusive prefix pre[0..B]
   {
-    const int per = (B + kThreads - 1) / kThreads;
-    const int lo = tid * per, hi = min(B, lo + per);
     int local = 0;
     unsigned flags = 0;
-    for (int i = lo; i < hi; ++i) {
-      const int len = p.seqlens[i];
-      if (len > p.Lmax) flags |= GQA_DEV_SEQLEN_CLAMPED;
-      if (len <= 0) flags |= GQA_DEV_EMPTY_CONTEXT;
-      local += (clamp_seq(len, p.Lmax) + kBN - 1) / kBN;
+#pragma unroll
+    for (int k = 0; k < kLensPerThread; ++k) {
+      if (lo + k < hi) {
+        if (lens[k] > p.Lmax) flags |= GQA_DEV_SEQLEN_CLAMPED;
+        if (lens[k] <= 0) flags |= GQA_DEV_EMPTY_CONTEXT;
+        local += (clamp_seq(lens[k], p.Lmax) + kBN - 1) / kBN;
+      }
     }
     if (flags && blockIdx.x == 0) atomicOr(p.err, flags);
     int incl = local;
@@ -217,25 +180,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     int run = scan[warp] + incl - local;
-    for (int i = lo; i < hi; ++i) {
-      pre[i] = run;
-      run += (clamp_seq(p.seqlens[i], p.Lmax) + kBN - 1) / kBN;
+#pragma unroll
+    for (int k = 0; k < kLensPerThread; ++k) {
+      if (lo + k < hi) {
+        pre[lo + k] = run;
+        run += (clamp_seq(lens[k], p.Lmax) + kBN - 1) / kBN;
+      }
     }
     if (lo < B && hi == B) pre[B] = run;
   }
   __syncthreads();
   const uint32_t tmem = *tmem_slot;
 
-  const long long T = (long long)Hkv * pre[B];
-  // CTAs that take a share: at most one per block; with many blocks, about
-  // six per CTA (longer shares mean fewer cut pairs and a gentler burst of
-  // ring fills at launch: a ragged MQA batch of 640 blocks ran in 28.7 us on
-  // 96 CTAs against 31.4 us on 148).  The others only zero-fill.
-  int P = (int)(T < p.num_ctas ? T : p.num_ctas);
-  if (T >= 2LL * p.num_ctas) P = (int)min((long long)P, (T + 5) / 6);
+  // Shares in 32-bit arithmetic (the host guarantees T < 2^31 / 160): no
+  // 64-bit division on the start-up path.  CTAs that take a share: at most
+  // one per block; with many blocks, about six per CTA (longer shares mean
+  // fewer cut pairs and a gentler burst of ring fills at launch: a ragged MQA
+  // batch of 640 blocks ran in 28.7 us on 96 CTAs against 31.4 us on 148).
+  // The others only zero-fill.
+  const int T = Hkv * pre[B];
+  int P = T < p.num_ctas ? T : p.num_ctas;
+  if (T >= 2 * p.num_ctas) P = min(P, (T + 5) / 6);
+  const Split sp = make_split(T, P);
   const bool active = (int)blockIdx.x < P;
-  const long long s_c = active ? T * blockIdx.x / P : 0;
-  const long long e_c = active ? T * (blockIdx.x + 1) / P : 0;
+  const int s_c = active ? share_start(sp, blockIdx.x) : 0;
+  const int e_c = active ? share_start(sp, blockIdx.x + 1) : 0;
 
   // Zero the outputs of sequences with an empty context.
   for (int b = blockIdx.x; b < B; b += p.num_ctas) {
@@ -244,10 +213,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = tid; e < p.Hq * kD; e += kThreads) o[e] = __float2bfloat16_rn(0.f);
   }
 
-  auto kslot = [&](long long i) { return (int)((2 * i) % p.stages); };
-  auto kpar = [&](long long i) { return (uint32_t)(((2 * i) / p.stages) & 1); };
-  auto vslot = [&](long long i) { return (int)((2 * i + 1) % p.stages); };
-  auto vpar = [&](long long i) { return (uint32_t)(((2 * i + 1) / p.stages) & 1); };
+  auto kslot = [&](int i) { return (2 * i) % p.stages; };
+  auto kpar = [&](int i) { return (uint32_t)(((2 * i) / p.stages) & 1); };
+  auto vslot = [&](int i) { return (2 * i + 1) % p.stages; };
+  auto vpar = [&](int i) { return (uint32_t)(((2 * i + 1) / p.stages) & 1); };
 
   if (warp == 0) {
     // ================================================================ producer
@@ -257,13 +226,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmV);
       const uint64_t pol = l2_policy_evict_first();
       Iter it;
-      it_seek(it, s_c, pre, B, Hkv);
+      it_seek32(it, s_c, pre, B, Hkv);
       int seg = 0;
-      long long issued = 0;
+      int issued = 0;
       bool ok = true;
       int pg_b = -1, pg_lp = -1, pg = 0;  // last block-table entry read (paged cache)
-      for (long long t = s_c; t < e_c && ok; ++t) {
-        const long long i = t - s_c;
+      for (int t = s_c; t < e_c && ok; ++t) {
+        const int i = t - s_c;
         const int z = it.b * Hkv + it.j;
         int kvz = z, kvy = it.lt * kBN;
         if (p.block_table) {
@@ -307,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         it_next(it, pre, B, Hkv);
       }
       // Drain: the last `stages` loads hold the latest use of every slot.
-      for (long long n = issued > p.stages ? issued - p.stages : 0; n < issued; ++n)
+      for (int n = issued > p.stages ? issued - p.stages : 0; n < issued; ++n)
         wait_drain(&kv_full[n % p.stages], (uint32_t)((n / p.stages) & 1), p.err);
       if (seg > 0) wait_drain(q_full, (seg - 1) & 1, p.err);
     }
@@ -326,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto commit = [&](uint64_t* bar) {
       if (leader) tc::commit(bar);
     };
-    auto issue_s = [&](long long i) {
+    auto issue_s = [&](int i) {
       const uint64_t b0 = dk + (uint64_t)((kslot(i) * kBlockBytes) >> 4);
       const uint32_t d = tmem + (uint32_t)(i & 1) * 128;
       if (leader) {
@@ -337,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    auto issue_pv = [&](long long i, bool acc) {
+    auto issue_pv = [&](int i, bool acc) {
       const uint64_t b0 = dv + (uint64_t)((vslot(i) * kBlockBytes) >> 4);
       const uint32_t a = tmem + (uint32_t)(i & 1) * 128;
       if (leader) {
@@ -347,12 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     Iter it;
-    if (s_c < e_c) it_seek(it, s_c, pre, B, Hkv);
+    if (s_c < e_c) it_seek32(it, s_c, pre, B, Hkv);
     int seg = 0;
     bool ok = true;
     bool prev_first = false, prev_last = false;
-    for (long long t = s_c; t < e_c && ok; ++t) {
-      const long long i = t - s_c;
+    for (int t = s_c; t < e_c && ok; ++t) {
+      const int i = t - s_c;
       const bool first = (t == s_c) || it.lt == 0;
       const bool last = (t == e_c - 1) || it.lt == it.nb - 1;
       if (first) {
@@ -384,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       it_next(it, pre, B, Hkv);
     }
     if (ok && e_c > s_c) {
-      const long long i = e_c - s_c;  // P V of the share's last block
+      const int i = e_c - s_c;  // P V of the share's last block
       ok = wait(&p_full[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1));
       if (ok) ok = wait(&kv_full[vslot(i - 1)], vpar(i - 1));
       if (ok) {
@@ -405,15 +374,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
     const uint32_t o_tm = tmem + lane_addr + kColO;
     Iter it;
-    if (s_c < e_c) it_seek(it, s_c, pre, B, Hkv);
+    if (s_c < e_c) it_seek32(it, s_c, pre, B, Hkv);
     int seg = 0, seg_lt0 = 0, len_b = 0;
     float m_use = -INFINITY, l = 0.f;
     // After a timeout the group keeps walking the share with every wait
     // returning at once (the abort flag is up), so that all four warps always
     // meet the same named barriers; only the memory work is skipped.
     bool ok = true;
-    for (long long t = s_c; t < e_c; ++t) {
-      const long long i = t - s_c;
+    for (int t = s_c; t < e_c; ++t) {
+      const int i = t - s_c;
       const bool first = (t == s_c) || it.lt == 0;
       const bool last = (t == e_c - 1) || it.lt == it.nb - 1;
       if (first) {
@@ -565,9 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // number of pieces merges them all.
           named_bar_sync(1, 128);
           if (r == 0 && !*abort_flag) {
-            const long long o_p = (long long)Hkv * pre[it.b] + (long long)it.j * it.nb;
-            const int c_lo = owner_cta(o_p, T, P);
-            const int c_hi = owner_cta(o_p + it.nb - 1, T, P);
+            const int o_p = Hkv * pre[it.b] + it.j * it.nb;
+            const int c_lo = share_owner(sp, o_p);
+            const int c_hi = share_owner(sp, o_p + it.nb - 1);
             const int pair = it.b * Hkv + it.j;
             const int old = atomic_add_acq_rel_gpu(&p.counters[pair], 1);
             const bool lastc = old == c_hi - c_lo;
@@ -580,108 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar_sync(1, 128);
           const int lf = *merge_flag;
           if (lf) {
-            // Merge all pieces of the pair.  Thread r covers head h0 + r / 4
-            // and columns [32 (r % 4), 32 (r % 4) + 32): one pass for the
-            // pieces' maxima, one for the weighted sums, with the loads of
-            // consecutive pieces in flight together.
             const int c_lo = lf - 1, nseg = *chi_flag - c_lo + 1;
-            // Up to kFastSeg pieces: every load of the thread's share is
-            // issued at once (one round trip to L2 -- the partials were
-            // written by other SMs, possibly on the other die) before any
-            // arithmetic; more pieces take the two-pass loop below.
-            constexpr int kFastSeg = 4;
-            for (int h0 = 0; h0 < G && nseg <= kFastSeg; h0 += 32) {
-              const int h = h0 + (r >> 2), cg = r & 3;
-              if (h < G) {
-                float ms[kFastSeg], ls[kFastSeg];
-                float4 x[kFastSeg][8];
-#pragma unroll
-                for (int s2 = 0; s2 < kFastSeg; ++s2) {
-                  if (s2 < nseg) {
-                    const size_t si = (size_t)(c_lo + s2) * 2 + (s2 == 0 ? 1 : 0);
-                    ms[s2] = __ldcg(p.part_ml + (si * 2 + 0) * G + h);
-                    ls[s2] = __ldcg(p.part_ml + (si * 2 + 1) * G + h);
-                    const float4* src = reinterpret_cast<const float4*>(p.part_acc + (si * G + h) * kD + cg * 32);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) x[s2][v] = __ldcg(src + v);
-                  } else {
-                    ms[s2] = -INFINITY;
-                    ls[s2] = 0.f;
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) x[s2][v] = make_float4(0.f, 0.f, 0.f, 0.f);
-                  }
-                }
-                float M = ms[0];
-#pragma unroll
-                for (int s2 = 1; s2 < kFastSeg; ++s2) M = fmaxf(M, ms[s2]);
-                const float Mu = M == -INFINITY ? 0.f : M;
-                float Ls = 0.f, f[kFastSeg];
-#pragma unroll
-                for (int s2 = 0; s2 < kFastSeg; ++s2) {
-                  f[s2] = fast_exp2(ms[s2] - Mu);
-                  Ls += f[s2] * ls[s2];
-                }
-                const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-                uint4* dst = reinterpret_cast<uint4*>(outp + (size_t)h * kD + cg * 32);
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-#pragma unroll
-                  for (int s2 = 0; s2 < kFastSeg; ++s2) {
-                    const float4 y0 = x[s2][2 * v], y1 = x[s2][2 * v + 1];
-                    a0.x += f[s2] * y0.x;
-                    a0.y += f[s2] * y0.y;
-                    a0.z += f[s2] * y0.z;
-                    a0.w += f[s2] * y0.w;
-                    a1.x += f[s2] * y1.x;
-                    a1.y += f[s2] * y1.y;
-                    a1.z += f[s2] * y1.z;
-                    a1.w += f[s2] * y1.w;
-                  }
-                  dst[v] = make_uint4(pack_bf16x2(a0.x * inv, a0.y * inv), pack_bf16x2(a0.z * inv, a0.w * inv),
-                                      pack_bf16x2(a1.x * inv, a1.y * inv), pack_bf16x2(a1.z * inv, a1.w * inv));
-                }
-              }
-            }
-            for (int h0 = 0; h0 < G && nseg > kFastSeg; h0 += 32) {
-              const int h = h0 + (r >> 2), cg = r & 3;
-              if (h < G) {
-                float M = -INFINITY;
-#pragma unroll 4
-                for (int s2 = 0; s2 < nseg; ++s2) {
-                  const size_t si = (size_t)(c_lo + s2) * 2 + (s2 == 0 ? 1 : 0);
-                  M = fmaxf(M, __ldcg(p.part_ml + (si * 2 + 0) * G + h));
-                }
-                const float Mu = M == -INFINITY ? 0.f : M;
-                float Ls = 0.f;
-                float4 acc4[8];
-#pragma unroll
-                for (int v = 0; v < 8; ++v) acc4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-                for (int s2 = 0; s2 < nseg; ++s2) {
-                  const size_t si = (size_t)(c_lo + s2) * 2 + (s2 == 0 ? 1 : 0);
-                  const float f = fast_exp2(__ldcg(p.part_ml + (si * 2 + 0) * G + h) - Mu);
-                  Ls += f * __ldcg(p.part_ml + (si * 2 + 1) * G + h);
-                  const float4* src = reinterpret_cast<const float4*>(p.part_acc + (si * G + h) * kD + cg * 32);
-#pragma unroll
-                  for (int v = 0; v < 8; ++v) {
-                    const float4 x = __ldcg(src + v);
-                    acc4[v].x += f * x.x;
-                    acc4[v].y += f * x.y;
-                    acc4[v].z += f * x.z;
-                    acc4[v].w += f * x.w;
-                  }
-                }
-                const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-                uint4* dst = reinterpret_cast<uint4*>(outp + (size_t)h * kD + cg * 32);
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                  const float4 a0 = acc4[2 * v], a1 = acc4[2 * v + 1];
-                  dst[v] = make_uint4(pack_bf16x2(a0.x * inv, a0.y * inv), pack_bf16x2(a0.z * inv, a0.w * inv),
-                                      pack_bf16x2(a1.x * inv, a1.y * inv), pack_bf16x2(a1.z * inv, a1.w * inv));
-                }
-              }
-            }
+            merge_pieces(p.part_acc, p.part_ml, G, c_lo, nseg, outp, r);
           }
           named_bar_sync(1, 128);
         }
@@ -714,9 +583,10 @@ bool decode_tc_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, Decod
   plan->tile_keys = kBN;
   plan->threads = kThreads;
   const long long blocks_max = (long long)B * Hkv * ((Lmax + kBN - 1) / kBN);
-  plan->num_ctas = (int)std::min<long long>(blocks_max, std::min(kMaxCtasTc, std::max(1, sm_count)));
+  if (blocks_max >= (1LL << 31) / kMaxCtas) return false;  // the kernel's split arithmetic is 32-bit
+  plan->num_ctas = (int)std::min<long long>(blocks_max, std::min(kMaxCtas, std::max(1, sm_count)));
   const TcLayout l0 = tc_layout(0);
-  int stages = (kSmemLimitTc - l0.total - 16 * 8) / kBlockBytes;
+  int stages = (kSmemLimit - l0.total - 16 * 8) / kBlockBytes;
   stages = std::min(stages, 8);
   if (stages < 2) return false;
   plan->stages = stages;
@@ -770,7 +640,7 @@ cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaSt
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !(attr_set.load() >> dev & 1ull)) {
-    e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimitTc);
+    e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set.fetch_or(1ull << dev);
   }

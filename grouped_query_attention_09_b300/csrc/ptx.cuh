@@ -66,6 +66,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe: true if the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this are a test's request to give up at once: the wait probes
+// without blocking and gives up the first time it finds the phase unfinished.
+constexpr unsigned long long kImmediateWaitNs = 1000ull;
+
 // Waits until the phase of `bar` with the given parity has completed.
 // Gives up after limit_ns, or as soon as *abort (shared) is non-zero: on
 // expiry it records GQA_DEV_WAIT_TIMEOUT in *err, raises *abort and returns
@@ -73,6 +90,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, unsigned* err,
                                                   unsigned long long limit_ns) {
+  if (limit_ns < kImmediateWaitNs) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (*abort) return false;
+    atomicOr(err, GQA_DEV_WAIT_TIMEOUT);
+    *abort = 1;
+    return false;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
@@ -190,6 +214,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 1/x on the SFU (rcp.approx.ftz, about 1 ulp).
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Device-scope atomic add with acquire-release semantics: the release
 // publishes every store ordered before it (including other threads' stores
 // ordered by a preceding barrier), the acquire makes other CTAs' published
@@ -240,6 +271,21 @@ __device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
       "mov.b64 {%0, %1}, rd;\n\t}"
       : "+f"(d0), "+f"(d1)
       : "f"(a0), "f"(a1));
+}
+
+// Named barrier over `nthreads` threads that also ORs `pred` over them: every
+// participant gets true if any passed true.
+__device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // Named barrier over `nthreads` threads (a multiple of 32).

@@ -329,7 +329,8 @@ GQA_API int gqa_decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int* tile_k
  * gqa_test_set_wait_limit_ns -- every pipeline wait (a producer waiting for a
  * free ring slot, a consumer for its data, the MMA issuer for the softmax)
  * of kernels launched after this call gives up after `ns` nanoseconds
- * instead of the default 2 s; 0 restores the default.  A wait that gives up
+ * instead of the default 2 s (a limit below 1000 ns gives up the first time a
+ * wait finds its data not ready); 0 restores the default.  A wait that gives up
  * sets GQA_DEV_WAIT_TIMEOUT and the kernel returns early with its output
  * invalid; nothing traps.  The waits with which a CTA lets its own copies and
  * MMAs land before it exits keep the 2 s limit.

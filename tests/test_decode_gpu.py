@@ -163,7 +163,9 @@ def test_side_stream_and_host_entry_point(gqa_lib, cuda_device):
     assert torch.equal(ref.cpu(), host)
 
 
-# ---- wide groups (G >= 16 at D = 128): the tcgen05 decode kernel
+# ---- wide groups (G > 8 at D = 128): the tcgen05 decode kernels, keys as
+# the MMA rows for G <= 32 (16 or 32 padded head columns), heads as the MMA
+# rows above
 
 @pytest.mark.parametrize("B,Hq,Hkv,Lmax,lens", [
     (3, 16, 1, 700, [700, 129, 1]),          # G = 16; one key; one past a block edge
@@ -172,6 +174,12 @@ def test_side_stream_and_host_entry_point(gqa_lib, cuda_device):
     (2, 64, 1, 1000, [1000, 513]),           # G = 64: two warps of heads
     (1, 128, 1, 384, [384]),                 # G = 128: every TMEM lane a head
     (4, 64, 2, 900, [900, 128, 127, 640]),   # G = 32, two KV heads; block-exact lengths
+    (2, 9, 1, 500, [500, 77]),               # G = 9: smallest group on the keys-in-M kernel
+    (2, 34, 2, 300, [300, 129]),             # G = 17: first group padded to 32 columns
+    (1, 33, 1, 256, [256]),                  # G = 33: smallest group with heads as the MMA rows
+    (5, 80, 4, 1500, [1500, 1, 384, 1023, 700]),  # G = 20, four KV heads (whole-pair shares)
+    (2, 32, 1, 8192, [8192, 300]),          # one long pair cut into many pieces (split shares, > 4 pieces)
+    (4, 64, 2, 4096, [4096, 100, 2000, 4096]),  # G = 32, split shares over every SM, cut pairs
 ])
 def test_wide_group_shapes(gqa_lib, oracle_mod, cuda_device, B, Hq, Hkv, Lmax, lens):
     w = W.DecodeWorkload("wide", B, Hq, Hkv, 128, Lmax, 1, Lmax, 2000 + B * Hq + Lmax)
