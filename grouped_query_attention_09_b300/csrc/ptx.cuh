@@ -214,13 +214,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// 1/x on the SFU (rcp.approx.ftz, about 1 ulp).
-__device__ __forceinline__ float fast_rcp(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Device-scope atomic add with acquire-release semantics: the release
 // publishes every store ordered before it (including other threads' stores
 // ordered by a preceding barrier), the acquire makes other CTAs' published
@@ -271,21 +264,6 @@ __device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
       "mov.b64 {%0, %1}, rd;\n\t}"
       : "+f"(d0), "+f"(d1)
       : "f"(a0), "f"(a1));
-}
-
-// Named barrier over `nthreads` threads that also ORs `pred` over them: every
-// participant gets true if any passed true.
-__device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
-      : "memory");
-  return r != 0;
 }
 
 // Named barrier over `nthreads` threads (a multiple of 32).

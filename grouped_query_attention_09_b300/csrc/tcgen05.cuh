@@ -40,12 +40,12 @@ __device__ __forceinline__ void fence_after_sync() {
 
 // ------------------------------------------------------------ descriptors
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator,
-// M x N tile.  b_mn_major / a_mn_major: B (A) is stored with N (M)
-// contiguous (MN-major) instead of K contiguous.  Bit layout: [4,6) D format
-// (1 = f32), [7,10) A format (1 = bf16), [10,13) B format (1 = bf16), 15 A
-// major, 16 B major, [17,23) N >> 3, [24,29) M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major, bool a_mn_major = false) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+// M x N tile.  b_mn_major: B is stored with N contiguous (MN-major) instead of
+// K contiguous.  Bit layout: [4,6) D format (1 = f32), [7,10) A format
+// (1 = bf16), [10,13) B format (1 = bf16), 15 A major, 16 B major,
+// [17,23) N >> 3, [24,29) M >> 4.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
@@ -119,16 +119,6 @@ __device__ __forceinline__ void ld_32x32b_x32(uint32_t taddr, uint32_t (&x)[32])
       : "r"(taddr));
 }
 
-// 32 lanes x 32 bits, repeated 16 times: thread i receives columns
-// [col, col + 16) of TMEM lane (lane base + i).
-__device__ __forceinline__ void ld_32x32b_x16(uint32_t taddr, uint32_t (&x)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]),
-        "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15])
-      : "r"(taddr));
-}
-
 __device__ __forceinline__ void st_32x32b_x32(uint32_t taddr, const uint32_t (&x)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
@@ -158,13 +148,6 @@ __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.
       "+r"(x[29]), "+r"(x[30]), "+r"(x[31])
 __device__ __forceinline__ void wait_ld_regs(uint32_t (&x)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : GQA_RW32(x)::"memory");
-}
-__device__ __forceinline__ void wait_ld_regs(uint32_t (&x)[16]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4]), "+r"(x[5]), "+r"(x[6]), "+r"(x[7]),
-                 "+r"(x[8]), "+r"(x[9]), "+r"(x[10]), "+r"(x[11]), "+r"(x[12]), "+r"(x[13]), "+r"(x[14]), "+r"(x[15])
-               :
-               : "memory");
 }
 // Ties further register arrays to an earlier wait (emits no instruction).
 __device__ __forceinline__ void pin_regs(uint32_t (&x)[32]) { asm volatile("" : GQA_RW32(x)); }
