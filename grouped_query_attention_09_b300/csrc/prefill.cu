@@ -411,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float x0, x1;
             fma2(x0, x1, __uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1]), sl, sl, nref, nref);
             const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            add2(ls[2 * (e & 3)], ls[2 * (e & 3) + 1], p0, p1);
+            ls[2 * (e & 3)] += p0;
+            ls[2 * (e & 3) + 1] += p1;
             pw[e] = pack_bf16x2(p0, p1);
           }
           tc::st_32x32b_x16(s_tm + c * 16, pw);
