@@ -975,12 +975,12 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
   if (B < 1 || B > kMaxBatch || Hkv < 1 || Hq % Hkv != 0 || Lmax < 1) return false;
   if (D != 64 && D != 128) return false;
   const int G = Hq / Hkv;
-  // An FP8 cache runs on the warp-level kernel, built for D = 128, G <= 8.
-  if (kv8 && (D != 128 || G > 8)) return false;
+  // An FP8 cache is built for D = 128.
+  if (kv8 && D != 128) return false;
   // Wide groups at D = 128 go to the tcgen05 kernel: its tensor core reads
   // each K/V block from shared memory once for all G heads.
-  if (!kv8 && D == 128 && G > 8 && G <= 128) {
-    if (!decode_tc_plan(B, Hq, Hkv, D, Lmax, sm_count, plan)) return false;
+  if (D == 128 && G > 8 && G <= 128) {
+    if (!decode_tc_plan(B, Hq, Hkv, D, Lmax, sm_count, plan, kv8)) return false;
     if (max_part_floats > 0 && plan->ws_part_floats > max_part_floats) return false;
     return true;
   }

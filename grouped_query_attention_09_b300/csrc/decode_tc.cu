@@ -58,6 +58,7 @@ constexpr int kThreads = 256;
 constexpr int kColO = 256;
 
 struct TcParams {
+  const __nv_bfloat16* q;  // read directly only for an FP8 cache (else through tmQ)
   __nv_bfloat16* out;
   const int32_t* seqlens;
   float* part_acc;  // [num_ctas][2][G][D]
@@ -69,31 +70,51 @@ struct TcParams {
   const int32_t* block_table;  // paged cache (else null): [B][max_pages]
   int page_size, max_pages, num_pages;
   unsigned long long wait_ns;  // pipeline-wait limit
+  // FP8 (E4M3) cache: per (b, kv head) scales of K and V, and the depth of
+  // the ring the E4M3 blocks land in before their conversion.
+  const float* k_scale;
+  const float* v_scale;
+  int stages8;
 };
+
+constexpr int kBlockBytes8 = kBN * kD;  // one E4M3 K or V block: 16 KiB
 
 struct TcLayout {
-  int ring_off, pre_off, bar_off, misc_off, total;
+  int ring_off, ring8_off, pre_off, bar_off, misc_off, total;
 };
 
-__host__ __device__ inline TcLayout tc_layout(int stages) {
+// stages: the ring the MMAs read (bf16, or fp16 converted from E4M3);
+// stages8: the ring E4M3 blocks land in (0 for a bf16 cache).
+__host__ __device__ inline TcLayout tc_layout(int stages, int stages8) {
   TcLayout l;
   l.ring_off = kQBytes;
-  l.pre_off = l.ring_off + stages * kBlockBytes;
+  l.ring8_off = l.ring_off + stages * kBlockBytes;
+  l.pre_off = l.ring8_off + stages8 * kBlockBytes8;
   l.bar_off = l.pre_off + ((kMaxBatch + 1) * 4 + 7) / 8 * 8;
-  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done, o_full, mma_done
-  l.misc_off = l.bar_off + (2 + 2 * stages + 2 + 2 + 3) * 8;
+  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done, o_full, mma_done,
+  // e8_full[S8], e8_empty[S8]
+  l.misc_off = l.bar_off + (2 + 2 * stages + 2 + 2 + 3 + 2 * stages8) * 8;
   l.total = l.misc_off + 4 * 40 + 1024;  // flags + scan scratch, + alignment slack
   return l;
 }
 
+// KV8: the cache holds E4M3 bytes.  The producer then lands each K or V
+// block in an E4M3 ring; warps 2-3 convert it (exactly) to fp16 in the
+// 128-byte-swizzled layout the MMAs read, zeroing the V rows past the
+// sequence end, and also write the pair's q as fp16 into the Q tile; the
+// MMAs run in fp16 (kind::f16 with f16 operands), P is fp16, the K scale
+// joins the logit scale and the V scale the output.
+template <bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const TcParams p) {
-  const TcLayout L = tc_layout(p.stages);
+  const int S8 = KV8 ? p.stages8 : 1;  // (1 keeps the bf16 instantiation free of a modulo by zero)
+  const TcLayout L = tc_layout(p.stages, KV8 ? p.stages8 : 0);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_tile = smem;
   uint8_t* ring = smem + L.ring_off;
+  uint8_t* ring8 = smem + L.ring8_off;
   int* pre = reinterpret_cast<int*>(smem + L.pre_off);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* q_full = bars;
@@ -105,6 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_done = p_full + 2;
   uint64_t* o_full = o_done + 1;
   uint64_t* mma_done = o_full + 1;
+  uint64_t* e8_full = mma_done + 1;   // [S8] an E4M3 block landed (KV8)
+  uint64_t* e8_empty = e8_full + S8;  // [S8] ... and was converted (KV8)
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
   volatile int* abort_flag = misc;
   volatile int* merge_flag = misc + 1;
@@ -123,12 +146,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int k = 0; k < kLensPerThread; ++k) lens[k] = (lo + k < hi) ? __ldg(p.seqlens + lo + k) : 0;
 
+  // With KV8 the Q tile and the blocks the MMAs read are written by the 64
+  // converter threads (warps 2-3) instead of by TMA.
+  constexpr int kConv = 64;
   if (tid == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_full, KV8 ? kConv : 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_full[s], KV8 ? kConv : 1);
       mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; KV8 && s < S8; ++s) {
+      mbar_init(&e8_full[s], 1);
+      mbar_init(&e8_empty[s], kConv);
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(&s_full[k], 1);
@@ -251,6 +281,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           kvz = pg < 0 ? -1 : pg * Hkv + it.j;
           kvy -= lp * p.page_size;
         }
+        if (KV8) {
+          // E4M3 blocks into their own ring; the converters take them on
+          for (int kv = 0; kv < 2 && ok; ++kv) {
+            const int n = 2 * i + kv, s8 = n % S8;
+            if (n >= S8) {
+              ok = mbar_wait_bounded(&e8_empty[s8], (uint32_t)(((n / S8) & 1) ^ 1), abort_flag, p.err, p.wait_ns);
+              if (!ok) break;
+            }
+            mbar_arrive_expect_tx(&e8_full[s8], kBlockBytes8);
+            tma_load_3d(ring8 + s8 * kBlockBytes8, kv ? &tmV : &tmK, 0, kvy, kvz, &e8_full[s8], pol);
+            issued = n + 1;
+          }
+          it_next(it, pre, B, Hkv);
+          continue;
+        }
         if (t == s_c || it.lt == 0) {
           ok = mbar_wait_bounded(q_empty, (seg & 1) ^ 1, abort_flag, p.err, p.wait_ns);
           if (!ok) break;
@@ -276,14 +321,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         it_next(it, pre, B, Hkv);
       }
       // Drain: the last `stages` loads hold the latest use of every slot.
-      for (int n = issued > p.stages ? issued - p.stages : 0; n < issued; ++n)
-        wait_drain(&kv_full[n % p.stages], (uint32_t)((n / p.stages) & 1), p.err);
-      if (seg > 0) wait_drain(q_full, (seg - 1) & 1, p.err);
+      if (KV8) {
+        for (int n = issued > S8 ? issued - S8 : 0; n < issued; ++n)
+          wait_drain(&e8_full[n % S8], (uint32_t)((n / S8) & 1), p.err);
+      } else {
+        for (int n = issued > p.stages ? issued - p.stages : 0; n < issued; ++n)
+          wait_drain(&kv_full[n % p.stages], (uint32_t)((n / p.stages) & 1), p.err);
+        if (seg > 0) wait_drain(q_full, (seg - 1) & 1, p.err);
+      }
     }
   } else if (warp == 1) {
     // ================================================================ MMA
-    constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kBN, false);
-    constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, kD, true);
+    constexpr uint32_t idesc_s = KV8 ? tc::idesc_f16_f32(128, kBN, false) : tc::idesc_bf16_f32(128, kBN, false);
+    constexpr uint32_t idesc_o = KV8 ? tc::idesc_f16_f32(128, kD, true) : tc::idesc_bf16_f32(128, kD, true);
     const bool leader = elect_one_sync();
     const uint64_t dq = tc::sdesc_sw128(smem_u32(q_tile), 16, 1024);
     const uint64_t dk = tc::sdesc_sw128(smem_u32(ring), 16, 1024);
@@ -366,6 +416,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     commit(mma_done);
     wait_drain(mma_done, 0, p.err);
+  } else if (KV8 && warp < 4) {
+    // ================================================================ E4M3 -> fp16 converters
+    const int ct = tid - 64;  // 0 .. 63
+    // Rows G..127 of the Q tile are padding MMA rows: zero once.
+    for (int e = ct; e < (128 - G) * 16; e += kConv) {
+      const int row = G + (e >> 4), c16 = e & 15;
+      *reinterpret_cast<uint4*>(q_tile + (c16 >> 3) * kHalf + row * 128 + (((c16 & 7) ^ (row & 7)) << 4)) =
+          make_uint4(0, 0, 0, 0);
+    }
+    Iter it;
+    if (s_c < e_c) it_seek32(it, s_c, pre, B, Hkv);
+    int seg = 0, len_b = 0;
+    bool ok = true;
+    for (int t = s_c; t < e_c && ok; ++t) {
+      const int i = t - s_c;
+      if (t == s_c || it.lt == 0) {
+        // The pair's query heads as fp16 rows of the Q tile (128-byte swizzle,
+        // two 64-column halves), once the previous piece's scores are done.
+        ok = mbar_wait_bounded(q_empty, (seg & 1) ^ 1, abort_flag, p.err, p.wait_ns);
+        if (!ok) break;
+        const __nv_bfloat16* qb = p.q + ((size_t)it.b * p.Hq + (size_t)it.j * G) * kD;
+        for (int e = ct; e < G * 16; e += kConv) {
+          const int row = e >> 4, c16 = e & 15;
+          const uint4 x = __ldg(reinterpret_cast<const uint4*>(qb + (size_t)row * kD + c16 * 8));
+          const uint4 h = make_uint4(
+              pack_f16x2(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xFFFF0000u)),
+              pack_f16x2(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xFFFF0000u)),
+              pack_f16x2(__uint_as_float(x.z << 16), __uint_as_float(x.z & 0xFFFF0000u)),
+              pack_f16x2(__uint_as_float(x.w << 16), __uint_as_float(x.w & 0xFFFF0000u)));
+          *reinterpret_cast<uint4*>(q_tile + (c16 >> 3) * kHalf + row * 128 + (((c16 & 7) ^ (row & 7)) << 4)) = h;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(q_full);
+        ++seg;
+        len_b = clamp_seq(p.seqlens[it.b], p.Lmax);
+      }
+      const int valid = min(kBN, len_b - it.lt * kBN);
+      for (int kv = 0; kv < 2 && ok; ++kv) {
+        const int n = 2 * i + kv, s8 = n % S8, s = n % p.stages;
+        ok = mbar_wait_bounded(&e8_full[s8], (uint32_t)((n / S8) & 1), abort_flag, p.err, p.wait_ns);
+        if (ok && n >= p.stages)
+          ok = mbar_wait_bounded(&kv_empty[s], (uint32_t)(((n / p.stages) & 1) ^ 1), abort_flag, p.err, p.wait_ns);
+        if (!ok) break;
+        // 16 E4M3 bytes (d = 16c .. 16c + 15 of row r) become two 16-byte
+        // fp16 chunks of the row's half c / 4.  V rows at and past the
+        // sequence end become zeros (the cache may hold NaN bytes there).
+        const uint8_t* src = ring8 + s8 * kBlockBytes8;
+        uint8_t* dst = ring + s * kBlockBytes;
+        const int zero_from = kv ? valid : kBN;
+#pragma unroll 4
+        for (int e = ct; e < kBN * 8; e += kConv) {
+          const int r = e >> 3, c = e & 7;
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+          if (r < zero_from) {
+            const uint4 w = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
+            e4m3x4_to_f16x2x2(w.x, lo.x, lo.y);
+            e4m3x4_to_f16x2x2(w.y, lo.z, lo.w);
+            e4m3x4_to_f16x2x2(w.z, hi.x, hi.y);
+            e4m3x4_to_f16x2x2(w.w, hi.z, hi.w);
+          }
+          uint8_t* row = dst + (c >> 2) * kHalf + r * 128;
+          const int cc = 2 * (c & 3);
+          *reinterpret_cast<uint4*>(row + ((cc ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&e8_empty[s8]);
+        mbar_arrive(&kv_full[s]);
+      }
+      it_next(it, pre, B, Hkv);
+    }
   } else if (warp >= 4) {
     // ================================================================ softmax + epilogue
     const int r = tid - 128;                 // query head within the group = TMEM lane
@@ -377,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (s_c < e_c) it_seek32(it, s_c, pre, B, Hkv);
     int seg = 0, seg_lt0 = 0, len_b = 0;
     float m_use = -INFINITY, l = 0.f;
+    float slp = p.scale_log2, v_mul = 1.f;  // logit scale, output factor (FP8 cache: times its scales)
     // After a timeout the group keeps walking the share with every wait
     // returning at once (the abort flag is up), so that all four warps always
     // meet the same named barriers; only the memory work is skipped.
@@ -390,6 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         len_b = clamp_seq(p.seqlens[it.b], p.Lmax);
         m_use = -INFINITY;
         l = 0.f;
+        if (KV8) {
+          slp = p.scale_log2 * __ldg(p.k_scale + it.b * Hkv + it.j);
+          v_mul = __ldg(p.v_scale + it.b * Hkv + it.j);
+        }
       }
       const int valid = min(kBN, len_b - it.lt * kBN);  // keys of this block that exist (>= 1)
       {
@@ -425,14 +551,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mxv[e] = m;
         }
         const float mx = fmaxf(fmax3(mxv[0], mxv[1], mxv[2]), fmax3(fmax3(mxv[3], mxv[4], mxv[5]), mxv[6], mxv[7]));
-        const float mxs = mx * p.scale_log2;
+        const float mxs = mx * slp;
         const bool rebase = mxs > m_use + kRebase;
         const bool any_rebase = __any_sync(0xffffffffu, rebase);
         const float m_new = rebase ? mxs : m_use;
         const float alpha = rebase ? fast_exp2(m_use - m_new) : 1.f;
         m_use = m_new;
         const float ref = m_use == -INFINITY ? 0.f : m_use;
-        const float sl = p.scale_log2, nref = -ref;
+        const float sl = slp, nref = -ref;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -443,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fma2(x0, x1, __uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1]), sl, sl, nref, nref);
             const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
             ls[e & 3] += p0 + p1;
-            pw[e] = pack_bf16x2(p0, p1);
+            pw[e] = KV8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
           tc::st_32x32b_x16(s_tm + c * 16, pw);
         }
@@ -466,9 +592,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::wait_st();
       }
-      if (valid < kBN) {
+      if (!KV8 && valid < kBN) {
         // Cache rows at and past seqlens[b] may hold anything (NaN included):
-        // zero them in the V block so that P = 0 there contributes exactly 0.
+        // zero them in the V block so that P = 0 there contributes exactly 0
+        // (an FP8 cache's converters already wrote zeros there).
         uint8_t* vb = ring + vslot(i) * kBlockBytes;
         const bool w = mbar_wait_bounded(&kv_full[vslot(i)], vpar(i), abort_flag, p.err, p.wait_ns);
         ok = __all_sync(0xffffffffu, w) && ok;
@@ -497,12 +624,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t slot_idx = (size_t)blockIdx.x * 2 + slot;
         __nv_bfloat16* outp = p.out + ((size_t)it.b * p.Hq + (size_t)it.j * G) * kD;
         if (rows && ok) {
-          const float inv = l > 0.f ? 1.f / l : 0.f;
+          // the partial and the output carry the V scale (1 for a bf16 cache)
+          const float inv = l > 0.f ? v_mul / l : 0.f;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
             tc::ld_32x32b_x32(o_tm + c * 32, o);
             tc::wait_ld_regs(o);
+            if (KV8 && !complete) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * v_mul);
+            }
             if (r < G) {
               if (complete) {
                 uint4* dst = reinterpret_cast<uint4*>(outp + (size_t)r * kD + c * 32);
@@ -570,11 +702,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-bool decode_tc_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan) {
+bool decode_tc_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan, bool kv8) {
   if (B < 1 || B > kMaxBatch || Hkv < 1 || Hq % Hkv != 0 || Lmax < 1 || D != kD) return false;
   const int G = Hq / Hkv;
   if (G < 1 || G > 128) return false;
   plan->kind = 1;
+  plan->kv8 = kv8;
   plan->D = D;
   plan->G = G;
   plan->Gpad = 128;
@@ -585,12 +718,21 @@ bool decode_tc_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, Decod
   const long long blocks_max = (long long)B * Hkv * ((Lmax + kBN - 1) / kBN);
   if (blocks_max >= (1LL << 31) / kMaxCtas) return false;  // the kernel's split arithmetic is 32-bit
   plan->num_ctas = (int)std::min<long long>(blocks_max, std::min(kMaxCtas, std::max(1, sm_count)));
-  const TcLayout l0 = tc_layout(0);
-  int stages = (kSmemLimit - l0.total - 16 * 8) / kBlockBytes;
-  stages = std::min(stages, 8);
-  if (stages < 2) return false;
+  const TcLayout l0 = tc_layout(0, 0);
+  int stages, stages8 = 0;
+  if (kv8) {
+    // three fp16 blocks for the MMAs (one K, V pair and the next K), the
+    // rest of shared memory for E4M3 blocks in flight from HBM
+    stages = 3;
+    stages8 = std::min((kSmemLimit - l0.total - stages * kBlockBytes - 32 * 8) / kBlockBytes8, 8);
+    if (stages8 < 2) return false;
+  } else {
+    stages = std::min((kSmemLimit - l0.total - 16 * 8) / kBlockBytes, 8);
+    if (stages < 2) return false;
+  }
   plan->stages = stages;
-  plan->smem_bytes = (size_t)tc_layout(stages).total;
+  plan->stages8 = stages8;
+  plan->smem_bytes = (size_t)tc_layout(stages, stages8).total;
   plan->ws_part_floats = (size_t)plan->num_ctas * 2 * G * (D + 2);
   plan->chunk_tiles = 0;
   plan->chunks_max = plan->num_ctas;
@@ -604,18 +746,25 @@ cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaSt
   const int G = plan.G;
   const bool paged = a.block_table != nullptr;
   if (paged && (a.page_size % kBN != 0 || a.page_size <= 0)) return cudaErrorInvalidValue;
+  if (plan.kv8 && (!a.k_scale || !a.v_scale || paged)) return cudaErrorInvalidValue;
   const uint64_t planes = paged ? (uint64_t)a.num_pages * a.Hkv : pairs;
   const uint64_t rows = paged ? (uint64_t)a.page_size : (uint64_t)a.Lmax;
   // Q viewed as [B * Hkv][G][D]: a 128-row box starting at row 0 reads the
-  // group's G heads and zero-fills rows G..127.
-  if (encode_tmap_bf16_3d(&tq, a.q, kD, (uint64_t)G, pairs, (uint64_t)kD * 2, (uint64_t)G * kD * 2, 64, 128, 1) !=
-          CUDA_SUCCESS ||
-      encode_tmap_bf16_3d(&tk, a.k_cache, kD, rows, planes, (uint64_t)kD * 2, rows * kD * 2, 64, kBN, 1) !=
-          CUDA_SUCCESS ||
-      encode_tmap_bf16_3d(&tv, a.v_cache, kD, rows, planes, (uint64_t)kD * 2, rows * kD * 2, 64, kBN, 1) !=
-          CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  // group's G heads and zero-fills rows G..127.  An E4M3 cache is a byte
+  // tensor: one 128-byte box (a whole row of D = 128) per K or V block.
+  CUresult r1 =
+      encode_tmap_bf16_3d(&tq, a.q, kD, (uint64_t)G, pairs, (uint64_t)kD * 2, (uint64_t)G * kD * 2, 64, 128, 1);
+  CUresult r2, r3;
+  if (plan.kv8) {
+    r2 = encode_tmap_u8_3d(&tk, a.k_cache, kD, rows, planes, (uint64_t)kD, rows * kD, kD, kBN, 1);
+    r3 = encode_tmap_u8_3d(&tv, a.v_cache, kD, rows, planes, (uint64_t)kD, rows * kD, kD, kBN, 1);
+  } else {
+    r2 = encode_tmap_bf16_3d(&tk, a.k_cache, kD, rows, planes, (uint64_t)kD * 2, rows * kD * 2, 64, kBN, 1);
+    r3 = encode_tmap_bf16_3d(&tv, a.v_cache, kD, rows, planes, (uint64_t)kD * 2, rows * kD * 2, 64, kBN, 1);
+  }
+  if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS || r3 != CUDA_SUCCESS) return cudaErrorInvalidValue;
   TcParams p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.seqlens = a.seqlens;
   p.part_acc = a.ws_part;
@@ -635,16 +784,21 @@ cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaSt
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
   p.wait_ns = pipeline_wait_limit_ns();
-  static std::atomic<unsigned long long> attr_set{0};
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  p.stages8 = plan.stages8;
+  auto kern = plan.kv8 ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+  static std::atomic<unsigned long long> attr_set[2] = {{0}, {0}};
+  std::atomic<unsigned long long>& done = attr_set[plan.kv8 ? 1 : 0];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(attr_set.load() >> dev & 1ull)) {
-    e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  if (dev >= 64 || !(done.load() >> dev & 1ull)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set.fetch_or(1ull << dev);
+    if (dev < 64) done.fetch_or(1ull << dev);
   }
-  decode_tc_kernel<<<plan.num_ctas, kThreads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
+  kern<<<plan.num_ctas, kThreads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

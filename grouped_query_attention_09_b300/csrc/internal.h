@@ -33,7 +33,7 @@ CUresult encode_tmap_u8_3d(CUtensorMap* map, const void* base, uint64_t dim0, ui
 // ------------------------------------------------------------------ decode
 struct DecodePlan {
   int kind;                // 0: warp-level MMA kernel (decode.cu), 1: tcgen05 kernel (decode_tc.cu)
-  bool kv8;                // FP8 E4M3 cache (warp-level kernel, D = 128, G <= 8)
+  bool kv8;                // FP8 E4M3 cache (D = 128)
   int D, G, Gpad, NT, HS;  // head dim, group size, padded group, n-tiles/warp, head slices
   int tile_keys;           // keys per pipeline tile
   int chunk_tiles;         // tiles per scheduling chunk (unit of work a CTA claims)
@@ -41,6 +41,7 @@ struct DecodePlan {
   int num_ctas;            // persistent CTAs
   int threads;             // threads per CTA
   int stages;              // pipeline depth
+  int stages8 = 0;         // tcgen05 kernel with an FP8 cache: depth of the E4M3 ring
   size_t smem_bytes;       // dynamic shared memory per CTA
   size_t ws_part_floats;   // partial-result floats (acc + m + l)
   size_t ws_counters;      // per-(b, kv head) arrival counters
@@ -76,9 +77,10 @@ struct DecodeArgs {
 
 cudaError_t decode_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream);
 
-// The tcgen05 decode for wide groups (D = 128, 1 <= G <= 128); decode_plan
-// routes G > 8 to it.  Same workspace layout as the warp-level kernel.
-bool decode_tc_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan);
+// The tcgen05 decode for wide groups (D = 128, 1 <= G <= 128, bf16 or FP8
+// E4M3 cache); decode_plan routes G > 8 to it.  Same workspace layout as the
+// warp-level kernel.
+bool decode_tc_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePlan* plan, bool kv8 = false);
 cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream);
 
 // ------------------------------------------------------------------ prefill

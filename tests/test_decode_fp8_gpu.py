@@ -24,9 +24,11 @@ def oracle_fp8(o, q, k8, v8, ks, vs, sl, scale):
                         sl.numpy(), scale)
 
 
-@pytest.mark.parametrize("name", ["llama3_8b", "llama2_70b"])
+@pytest.mark.parametrize("name", ["llama3_8b", "llama2_70b", "mqa"])
 def test_fp8_workload_parity_full(gqa_lib, oracle_mod, cuda_device, name):
-    """Every output element of the Llama-shaped workloads with the cache in FP8."""
+    """Every output element of the Llama-shaped workloads and of the ragged
+    MQA batch (G = 32: the tcgen05 kernel with its E4M3 -> fp16 converter
+    warps) with the cache in FP8."""
     w = W.WORKLOADS[name]
     q, k8, v8, ks, vs, sl = W.make_decode_fp8_inputs(w)
     out, flags = run_fp8(gqa_lib, q, k8, v8, ks, vs, sl, w.scale, cuda_device)
@@ -40,6 +42,13 @@ def test_fp8_workload_parity_full(gqa_lib, oracle_mod, cuda_device, name):
     (4, 4, 4, 257, [63, 64, 65, 257]),    # MHA endpoint; tile boundaries
     (2, 6, 2, 300, [300, 17]),            # G = 3
     (1, 1, 1, 3000, [2999]),              # one head, long
+    (3, 16, 1, 700, [700, 129, 1]),       # G = 16 (tcgen05 kernel): one key; one past a block edge
+    (2, 24, 1, 400, [400, 255]),          # G = 24
+    (3, 36, 3, 260, [260, 1, 200]),       # G = 12
+    (2, 64, 1, 1000, [1000, 513]),        # G = 64
+    (1, 128, 1, 384, [384]),              # G = 128: every TMEM lane a head
+    (2, 32, 1, 8192, [8192, 300]),        # one long pair cut into many pieces (> 4-piece merge)
+    (4, 64, 2, 4096, [4096, 100, 2000, 4096]),  # G = 32 over every SM, cut pairs
 ])
 def test_fp8_shapes(gqa_lib, oracle_mod, cuda_device, B, Hq, Hkv, Lmax, lens):
     w = W.DecodeWorkload("fp8", B, Hq, Hkv, 128, Lmax, 1, Lmax, 3000 + B * Hq + Lmax)
@@ -68,10 +77,12 @@ def test_fp8_nan_tail_peaky_and_edges(gqa_lib, oracle_mod, cuda_device):
     assert_parity(out[keep], ref[keep], "fp8 edges")
 
 
-def test_fp8_scales_and_repeat(gqa_lib, cuda_device):
+@pytest.mark.parametrize("Hq,Hkv", [(16, 2), (32, 1)])
+def test_fp8_scales_and_repeat(gqa_lib, cuda_device, Hq, Hkv):
     """Doubling every V scale doubles the output (to bf16 rounding); two calls
-    give identical bits; wide groups are rejected."""
-    w = W.DecodeWorkload("fp8_scale", 4, 16, 2, 128, 600, 1, 600, 99)
+    give identical bits (the warp-level kernel at G = 8, the tcgen05 kernel
+    at G = 32)."""
+    w = W.DecodeWorkload("fp8_scale", 4, Hq, Hkv, 128, 600, 1, 600, 99)
     q, k8, v8, ks, vs, sl = [t.to(cuda_device) for t in W.make_decode_fp8_inputs(w)]
     a = gqa_lib.gqa_decode_fp8(q, k8, v8, ks, vs, sl).clone()
     b = gqa_lib.gqa_decode_fp8(q, k8, v8, ks, vs, sl).clone()
@@ -80,8 +91,34 @@ def test_fp8_scales_and_repeat(gqa_lib, cuda_device):
     d = gqa_lib.gqa_decode_fp8(q, k8, v8, ks, 2 * vs, sl)
     torch.cuda.synchronize()
     assert torch.allclose(d.float(), 2 * a.float(), rtol=2 ** -7, atol=1e-6)
-    wide = W.DecodeWorkload("fp8_wide", 2, 32, 1, 128, 256, 1, 256, 100)
-    qw, k8w, v8w, ksw, vsw, slw = [t.to(cuda_device) for t in W.make_decode_fp8_inputs(wide)]
+    assert gqa_lib.gqa_get_device_status() == 0
+
+
+def test_fp8_wide_group_nan_tail_and_edges(gqa_lib, oracle_mod, cuda_device):
+    """G = 32: E4M3 NaN bytes past every sequence end (the converter warps
+    must write zeros for those V rows), q x 8, an empty context and a clamped
+    length in one batch."""
+    w = W.DecodeWorkload("fp8_wide_edges", 6, 32, 1, 128, 1024, 1, 1024, 101)
+    sl = torch.tensor([1024, 1, 700, 0, 5000, 333], dtype=torch.int32)
+    q, k8, v8, ks, vs, _ = W.make_decode_fp8_inputs(w, q_mult=8.0)
+    for b in range(6):
+        n = int(sl[b].clamp(0, 1024))
+        k8[b, :, n:, :] = W.E4M3_NAN
+        v8[b, :, n:, :] = W.E4M3_NAN
+    out, flags = run_fp8(gqa_lib, q, k8, v8, ks, vs, sl, w.scale, cuda_device)
+    assert flags == (gqa_lib.GQA_DEV_EMPTY_CONTEXT | gqa_lib.GQA_DEV_SEQLEN_CLAMPED)
+    assert np.all(out[3] == 0)
+    ref = oracle_fp8(oracle_mod, q, k8, v8, ks, vs, sl.clamp(min=1, max=1024), w.scale)
+    keep = [0, 1, 2, 4, 5]
+    assert_parity(out[keep], ref[keep], "fp8 wide edges")
+
+
+def test_fp8_rejects_d64(gqa_lib, cuda_device):
+    w = W.DecodeWorkload("fp8_d64", 2, 8, 2, 64, 128, 1, 128, 102)
+    q = torch.zeros(2, 8, 64, dtype=torch.bfloat16, device=cuda_device)
+    k8 = torch.zeros(2, 2, 128, 64, dtype=torch.uint8, device=cuda_device)
+    sc = torch.ones(2, 2, device=cuda_device)
+    sl = torch.full((2,), 128, dtype=torch.int32, device=cuda_device)
     with pytest.raises(gqa_lib.GQAError) as e:
-        gqa_lib.gqa_decode_fp8(qw, k8w, v8w, ksw, vsw, slw)
+        gqa_lib.gqa_decode_fp8(q, k8, k8, sc, sc, sl, scale=w.scale)
     assert e.value.status == gqa_lib.GQA_ERR_UNSUPPORTED
