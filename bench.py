@@ -47,16 +47,13 @@ if ROOT not in sys.path:
 METRIC = "GQA decode K/V-read GB/s (% HBM peak); causal prefill TFLOP/s; 1xB300"
 HEADLINE = "llama3_8b"
 
-# DRAM bytes (read + write) per launch from one ncu capture, keyed by the
-# SHA-256 of the kernel source they were taken on; reported as null as soon
-# as the source differs.
+# DRAM bytes (read + write) per launch from one ncu capture of a workload,
+# keyed by the SHA-256 of the kernel source they were taken on; reported as
+# null as soon as the source differs.
 NCU_TRAFFIC = {
-    "decode.cu": {"sha256": "487aa1b48589117f81ae4df550c26e5fafec97a28c17783080bb6f11916c8c08",
-                  "bytes_per_launch": 271471104.0,
-                  "capture": "ncu --set full, llama3_8b decode (dram__bytes_read.sum + dram__bytes_write.sum); the source changed since only in comments and host-side plan code (identical cubin)"},
-    "prefill.cu": {"sha256": "ca3f3d65e2542ced2179f6472590ec6bd394e80cff71a988b85ce30b2ae7cd17",
-                   "bytes_per_launch": 115492864.0,
-                   "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, causal prefill B=4 L=2048"},
+    ("decode.cu", "llama3_8b"): {"sha256": "", "bytes_per_launch": None, "capture": ""},
+    ("decode_tc.cu", "mqa"): {"sha256": "", "bytes_per_launch": None, "capture": ""},
+    ("prefill.cu", "prefill"): {"sha256": "", "bytes_per_launch": None, "capture": ""},
 }
 
 
@@ -65,11 +62,15 @@ def _sha(path):
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def traffic_for(kernel_file, scale=1.0):
-    rec = NCU_TRAFFIC.get(os.path.basename(kernel_file))
-    if not rec or rec["sha256"] != _sha(kernel_file):
+def traffic_for(kernel_file, workload):
+    rec = NCU_TRAFFIC.get((os.path.basename(kernel_file), workload))
+    if not rec or not rec["bytes_per_launch"] or rec["sha256"] != _sha(kernel_file):
         return None
-    return rec["bytes_per_launch"] * scale
+    return rec["bytes_per_launch"]
+
+
+def _csrc(name):
+    return os.path.join(ROOT, "grouped_query_attention_09_b300", "csrc", name)
 
 
 def load_peaks():
@@ -510,11 +511,14 @@ def main():
             gbs = r["bytes"] / (ms / 1e3) / 1e9
             dw[name] = {"us": ms * 1e3, "kv_bytes": r["bytes"], "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
                         "TFLOP/s": r["flops"] / (ms / 1e3) / 1e12}
+            if name == "mqa":
+                dw[name]["kernel"] = "decode_tc_kernel<false>"
+                dw[name]["traffic"] = traffic_for(_csrc("decode_tc.cu"), "mqa")
         dw[HEADLINE] = {"us": mean_ms * 1e3, "kv_bytes": res["bytes"], "GB/s": achieved,
                         "frac_hbm": achieved / peaks["hbm_gbs"], "TFLOP/s": res["flops"] / (mean_ms / 1e3) / 1e12}
         extras["decode_workloads"] = dw
         d8 = {}
-        for name in ("llama3_8b", "llama2_70b"):
+        for name in ("llama3_8b", "llama2_70b", "mqa"):
             r = bench_decode_fp8(g, W, name, dev, small_steps, args.warmup, flush)
             ms = statistics.mean(r["ms"])
             gbs = r["bytes"] / (ms / 1e3) / 1e9
@@ -552,8 +556,7 @@ def main():
                              "frac": tf / peaks["bf16_tflops"],
                              "frac_sustained": tf / peaks["bf16_tflops_sustained"]
                              if peaks.get("bf16_tflops_sustained") else None,
-                             "traffic": traffic_for(os.path.join(ROOT, "grouped_query_attention_09_b300", "csrc",
-                                                                 "prefill.cu"))}}
+                             "traffic": traffic_for(_csrc("prefill.cu"), "prefill")}}
         else:
             extras["prefill"] = {"status": "not built"}
         pc = bench_prefill_chunk(g, W, dev, small_steps, args.warmup, flush)
@@ -581,8 +584,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
                          "kernel": "decode_kernel<128,1>",
-                         "traffic": traffic_for(os.path.join(ROOT, "grouped_query_attention_09_b300", "csrc",
-                                                             "decode.cu"))},
+                         "traffic": traffic_for(_csrc("decode.cu"), HEADLINE)},
             "cpu_baseline": cpu,
             "e2e": extras.pop("e2e", None),
             "gpu_launches": args.steps,

@@ -344,8 +344,8 @@ def gqa_release():
 
 
 def gqa_test_set_wait_limit_ns(ns: int):
-    """Test hook: pipeline waits of later launches give up after ns
-    nanoseconds (0 restores the default 2 s)."""
+    """Test hook: with ns > 0, later launches issue no pipeline loads and their
+    pipeline waits give up after ns nanoseconds (0 restores normal operation)."""
     load_library().gqa_test_set_wait_limit_ns(int(ns))
 
 

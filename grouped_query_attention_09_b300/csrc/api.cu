@@ -181,6 +181,8 @@ unsigned long long pipeline_wait_limit_ns() {
   return v ? v : kWaitLimitNs;
 }
 
+bool pipeline_starved() { return g_wait_limit_ns.load(std::memory_order_relaxed) != 0; }
+
 bool take_injected_alloc_failure() {
   int n = g_fail_allocs.load();
   while (n > 0)

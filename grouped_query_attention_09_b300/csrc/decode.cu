@@ -80,6 +80,7 @@ struct Params {
   int page_size, max_pages, num_pages;
   int prefetch_tiles;  // > 0: one CTA per (b, kv head) pair; prefetch its first tiles into L2 at launch
   unsigned long long wait_ns;  // pipeline-wait limit
+  int starve;                  // test hook: the producer issues no loads
 };
 
 struct SmemLayout {
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(288, 1)
 
   if (warp == NC) {
     // ============================== producer ==============================
-    if (lane == 0 && s_c < e_c) {
+    if (lane == 0 && s_c < e_c && !p.starve) {
       const uint64_t pol = l2_policy_evict_first();
       TileIter it;
       iter_seek(it, s_c, pre, B, Hkv);
@@ -949,6 +950,7 @@ cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t s
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
   p.wait_ns = pipeline_wait_limit_ns();
+  p.starve = pipeline_starved() ? 1 : 0;
   p.prefetch_tiles = 0;
   if (!a.block_table && plan.num_ctas == a.B * a.Hkv)
     p.prefetch_tiles = std::min(plan.stages, (a.Lmax + kBN - 1) / kBN);

@@ -70,6 +70,7 @@ struct TcParams {
   const int32_t* block_table;  // paged cache (else null): [B][max_pages]
   int page_size, max_pages, num_pages;
   unsigned long long wait_ns;  // pipeline-wait limit
+  int starve;                  // test hook: the producer issues no loads
   // FP8 (E4M3) cache: per (b, kv head) scales of K and V, and the depth of
   // the ring the E4M3 blocks land in before their conversion.
   const float* k_scale;
@@ -223,14 +224,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   // Shares in 32-bit arithmetic (the host guarantees T < 2^31 / 160): no
-  // 64-bit division on the start-up path.  CTAs that take a share: at most
-  // one per block; with many blocks, about six per CTA (longer shares mean
-  // fewer cut pairs and a gentler burst of ring fills at launch: a ragged MQA
-  // batch of 640 blocks ran in 28.7 us on 96 CTAs against 31.4 us on 148).
-  // The others only zero-fill.
+  // 64-bit division on the start-up path.  CTAs that take a share: about one
+  // per six blocks, at most one per SM.  Longer shares mean fewer cut pairs
+  // (each a merge through L2) and a gentler burst of ring fills at launch; a
+  // sweep over ragged G = 32 batches of 134 to 1018 blocks put six blocks per
+  // CTA within a few percent of the best count at every size (134 blocks:
+  // 25.6 us on 23 CTAs against 30.5 us on 134; 287 blocks: 26.8 us on 48
+  // against 33.3 us on 148).  The others only zero-fill.
   const int T = Hkv * pre[B];
-  int P = T < p.num_ctas ? T : p.num_ctas;
-  if (T >= 2 * p.num_ctas) P = min(P, (T + 5) / 6);
+  const int P = min(p.num_ctas, (T + 5) / 6);
   const Split sp = make_split(T, P);
   const bool active = (int)blockIdx.x < P;
   const int s_c = active ? share_start(sp, blockIdx.x) : 0;
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ================================================================ producer
-    if (lane == 0 && s_c < e_c) {
+    if (lane == 0 && s_c < e_c && !p.starve) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
@@ -784,6 +786,7 @@ cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaSt
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
   p.wait_ns = pipeline_wait_limit_ns();
+  p.starve = pipeline_starved() ? 1 : 0;
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
   p.stages8 = plan.stages8;

@@ -9,8 +9,11 @@
 namespace gqa {
 
 // Limit of the kernels' pipeline waits for launches made now (nanoseconds):
-// kWaitLimitNs unless gqa_test_set_wait_limit_ns chose another.
+// kWaitLimitNs unless gqa_test_set_wait_limit_ns chose another; in that case
+// pipeline_starved() is true and the kernels' producers issue no loads, so
+// that the waits for them run out.
 unsigned long long pipeline_wait_limit_ns();
+bool pipeline_starved();
 
 // Test hook of gqa_test_fail_workspace_allocs: true if this workspace
 // allocation is to fail (consumes one of the requested failures).

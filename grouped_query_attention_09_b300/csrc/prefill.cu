@@ -90,6 +90,7 @@ struct Params {
   float scale_log2;  // (1 / sqrt(D)) * log2(e)
   unsigned* err;
   unsigned long long wait_ns;  // pipeline-wait limit
+  int starve;                  // test hook: the producer issues no loads
 };
 
 struct Unit {
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && !p.starve) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -507,6 +508,7 @@ cudaError_t prefill_launch(const PrefillArgs& a, int sm_count, cudaStream_t stre
   p.scale_log2 = (1.0f / sqrtf((float)a.D)) * 1.4426950408889634f;
   p.err = a.err;
   p.wait_ns = pipeline_wait_limit_ns();
+  p.starve = pipeline_starved() ? 1 : 0;
   static std::atomic<unsigned long long> attr_set{0};  // one bit per device ordinal < 64
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

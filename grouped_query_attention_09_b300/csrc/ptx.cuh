@@ -15,9 +15,9 @@ namespace gqa {
 
 // How long a pipeline wait may spin before it gives up and flags
 // GQA_DEV_WAIT_TIMEOUT (nanoseconds of %globaltimer).  Kernels take their
-// pipeline-wait limit as a launch parameter (this value unless a test sets a
-// shorter one); the waits that drain in-flight copies and MMAs before a CTA
-// exits always use this value.
+// pipeline-wait limit as a launch parameter (this value unless a test sets
+// another); the waits that drain in-flight copies and MMAs before a CTA exits
+// always use this value.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -66,23 +66,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking probe: true if the phase with the given parity has completed.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Limits below this are a test's request to give up at once: the wait probes
-// without blocking and gives up the first time it finds the phase unfinished.
-constexpr unsigned long long kImmediateWaitNs = 1000ull;
-
 // Waits until the phase of `bar` with the given parity has completed.
 // Gives up after limit_ns, or as soon as *abort (shared) is non-zero: on
 // expiry it records GQA_DEV_WAIT_TIMEOUT in *err, raises *abort and returns
@@ -90,16 +73,9 @@ constexpr unsigned long long kImmediateWaitNs = 1000ull;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, unsigned* err,
                                                   unsigned long long limit_ns) {
-  if (limit_ns < kImmediateWaitNs) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if (*abort) return false;
-    atomicOr(err, GQA_DEV_WAIT_TIMEOUT);
-    *abort = 1;
-    return false;
-  }
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;

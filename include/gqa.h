@@ -329,14 +329,14 @@ GQA_API int gqa_decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int* tile_k
  * Test hooks: failure injection for the error paths (the paper pages have
  * no counterpart).  Not for production use.
  *
- * gqa_test_set_wait_limit_ns -- every pipeline wait (a producer waiting for a
- * free ring slot, a consumer for its data, the MMA issuer for the softmax)
- * of kernels launched after this call gives up after `ns` nanoseconds
- * instead of the default 2 s (a limit below 1000 ns gives up the first time a
- * wait finds its data not ready); 0 restores the default.  A wait that gives up
- * sets GQA_DEV_WAIT_TIMEOUT and the kernel returns early with its output
- * invalid; nothing traps.  The waits with which a CTA lets its own copies and
- * MMAs land before it exits keep the 2 s limit.
+ * gqa_test_set_wait_limit_ns -- with ns > 0, kernels launched after this
+ * call issue none of their pipeline loads (the TMA copies of Q, K and V) and
+ * every pipeline wait (a consumer waiting for its data, the MMA issuer for
+ * the softmax, ...) gives up after ns nanoseconds instead of the default
+ * 2 s: the waits for the loads that never come run out, the kernel sets
+ * GQA_DEV_WAIT_TIMEOUT and returns early with its output invalid; nothing
+ * traps.  The waits with which a CTA lets its own copies and MMAs land
+ * before it exits keep the 2 s limit.  0 restores normal operation.
  *
  * gqa_test_fail_workspace_allocs -- the next `n` allocations of the decode
  * workspace (made when a decode needs a larger one) fail as out of memory

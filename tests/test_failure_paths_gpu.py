@@ -1,13 +1,14 @@
 """Failure paths on the GPU, made to happen without a fault: a pipeline wait
 that runs out, and a workspace allocation that fails.
 
-The waits: gqa_test_set_wait_limit_ns(1) makes every pipeline wait of the
-next launches give up at its first check of the clock, so a full-size call
-takes the kernels' abort path (flag GQA_DEV_WAIT_TIMEOUT, every role leaves
-its loop, in-flight copies and MMAs are drained with the normal limit, TMEM is
-freed, the kernel returns).  The tests check that the call returns, that the
-status comes back, that reading it resets the decode workspace's arrival
-counters, and that the next normal call is parity-green against the oracle.
+The waits: gqa_test_set_wait_limit_ns(ns) makes the next launches issue no
+pipeline loads and give up every pipeline wait after ns, so the waits for
+data that never comes run out and the call takes the kernels' abort path
+(flag GQA_DEV_WAIT_TIMEOUT, every role leaves its loop, in-flight MMAs are
+drained with the normal limit, TMEM is freed, the kernel returns).  The tests
+check that the call returns, that the status comes back, that reading it
+resets the decode workspace's arrival counters, and that the next normal call
+is parity-green against the oracle.
 
 The allocation: gqa_test_fail_workspace_allocs(1) makes the next decode
 workspace allocation fail as out of memory; the call must return
@@ -22,10 +23,12 @@ from parity import assert_parity
 
 pytestmark = pytest.mark.gpu
 
+LIMIT_NS = 5_000_000  # 5 ms: each timed-out launch ends in about this long
+
 
 @pytest.fixture
 def short_waits(gqa_lib):
-    gqa_lib.gqa_test_set_wait_limit_ns(1)
+    gqa_lib.gqa_test_set_wait_limit_ns(LIMIT_NS)
     try:
         yield
     finally:
@@ -46,7 +49,7 @@ def test_decode_wait_timeout_then_recovers(gqa_lib, oracle_mod, cuda_device, nam
     d = cuda_device
     qd, kd, vd, sld = q.to(d), k.to(d), v.to(d), sl.to(d)
     assert gqa_lib.gqa_get_device_status() == 0
-    gqa_lib.gqa_test_set_wait_limit_ns(1)
+    gqa_lib.gqa_test_set_wait_limit_ns(LIMIT_NS)
     try:
         for _ in range(2):
             gqa_lib.gqa_decode(qd, kd, vd, sld, scale=w.scale)
@@ -63,11 +66,15 @@ def test_decode_wait_timeout_then_recovers(gqa_lib, oracle_mod, cuda_device, nam
 
 
 def test_fp8_and_paged_decode_wait_timeout(gqa_lib, cuda_device, short_waits):
-    w = W.WORKLOADS["llama3_8b"]
+    """FP8 caches on both kernels (the tcgen05 one waits in its converter
+    warps), and a paged cache."""
     d = cuda_device
-    q, k8, v8, ks, vs, sl = W.make_decode_fp8_inputs(w)
-    gqa_lib.gqa_decode_fp8(q.to(d), k8.to(d), v8.to(d), ks.to(d), vs.to(d), sl.to(d), scale=w.scale)
-    assert gqa_lib.gqa_get_device_status() & gqa_lib.GQA_DEV_WAIT_TIMEOUT
+    for name in ("llama3_8b", "mqa"):
+        w = W.WORKLOADS[name]
+        q, k8, v8, ks, vs, sl = W.make_decode_fp8_inputs(w)
+        gqa_lib.gqa_decode_fp8(q.to(d), k8.to(d), v8.to(d), ks.to(d), vs.to(d), sl.to(d), scale=w.scale)
+        assert gqa_lib.gqa_get_device_status() & gqa_lib.GQA_DEV_WAIT_TIMEOUT
+    w = W.WORKLOADS["llama3_8b"]
     q, k, v, sl = W.make_decode_inputs(w)
     kp, vp, bt = W.page_cache(k, v, 256, seed=3)
     gqa_lib.gqa_decode_paged(q.to(d), kp.to(d), vp.to(d), bt.to(d), sl.to(d), scale=w.scale)
@@ -79,7 +86,7 @@ def test_prefill_wait_timeout_then_recovers(gqa_lib, oracle_mod, cuda_device):
     q, k, v = W.make_prefill_inputs(w)
     d = cuda_device
     qd, kd, vd = q.to(d), k.to(d), v.to(d)
-    gqa_lib.gqa_test_set_wait_limit_ns(1)
+    gqa_lib.gqa_test_set_wait_limit_ns(LIMIT_NS)
     try:
         gqa_lib.gqa_prefill(qd, kd, vd, causal=True)
         gqa_lib.gqa_prefill_chunk(qd[:, :, 512:].contiguous(), kd, vd, causal=True)
