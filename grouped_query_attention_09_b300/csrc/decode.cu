@@ -516,7 +516,6 @@ __global__ void __launch_bounds__(288, 1)
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
-#pragma unroll
         float sc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // two MMA chains (even, odd k-steps)
         if constexpr (KV8) {
           // k-step kk: rows g and g + 8 of word kk % 4 of chunk 4 (kk / 4) + c;

@@ -93,8 +93,8 @@ __host__ __device__ inline TcLayout tc_layout(int stages, int stages8) {
   l.pre_off = l.ring8_off + stages8 * kBlockBytes8;
   l.bar_off = l.pre_off + ((kMaxBatch + 1) * 4 + 7) / 8 * 8;
   // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done, o_full, mma_done,
-  // e8_full[S8], e8_empty[S8]
-  l.misc_off = l.bar_off + (2 + 2 * stages + 2 + 2 + 3 + 2 * stages8) * 8;
+  // e8_full[S8], e8_empty[S8], pub_full[2]
+  l.misc_off = l.bar_off + (2 + 2 * stages + 2 + 2 + 3 + 2 * stages8 + 2) * 8;
   l.total = l.misc_off + 4 * 40 + 1024;  // flags + scan scratch, + alignment slack
   return l;
 }
@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* mma_done = o_full + 1;
   uint64_t* e8_full = mma_done + 1;   // [S8] an E4M3 block landed (KV8)
   uint64_t* e8_empty = e8_full + S8;  // [S8] ... and was converted (KV8)
+  uint64_t* pub_full = e8_empty + S8;  // [2] partial slot 0 / 1 written (bf16 cache: merged by warps 2-3)
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
   volatile int* abort_flag = misc;
   volatile int* merge_flag = misc + 1;
@@ -168,6 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(o_done, 1);
     mbar_init(o_full, 1);
     mbar_init(mma_done, 1);
+    mbar_init(&pub_full[0], 128);
+    mbar_init(&pub_full[1], 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -244,6 +247,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     __nv_bfloat16* o = p.out + (size_t)b * p.Hq * kD;
     for (int e = tid; e < p.Hq * kD; e += kThreads) o[e] = __float2bfloat16_rn(0.f);
   }
+
+  // The piece of pair (it.b, it.j) that ends here sits in this CTA's partial
+  // slot: count it in; the CTA whose piece completes the pair's count merges
+  // all the pieces into the output.  Run by the nthr threads r = 0 .. nthr-1
+  // that meet at named barrier bar_id (every one of them, also after an
+  // abort, so that the barrier counts always match).
+  auto publish_merge = [&](const Iter& it, __nv_bfloat16* outp, int r, int nthr, int bar_id) {
+    named_bar_sync(bar_id, nthr);
+    if (r == 0 && !*abort_flag) {
+      const int o_p = Hkv * pre[it.b] + it.j * it.nb;
+      const int c_lo = share_owner(sp, o_p);
+      const int c_hi = share_owner(sp, o_p + it.nb - 1);
+      const int pair = it.b * Hkv + it.j;
+      const int old = atomic_add_acq_rel_gpu(&p.counters[pair], 1);
+      const bool lastc = old == c_hi - c_lo;
+      if (lastc) p.counters[pair] = 0;  // ready for the next call (ordered by the kernel boundary)
+      *merge_flag = lastc ? c_lo + 1 : 0;
+      *chi_flag = c_hi;
+    } else if (r == 0) {
+      *merge_flag = 0;
+    }
+    named_bar_sync(bar_id, nthr);
+    const int lf = *merge_flag;
+    if (lf) {
+      const int c_lo = lf - 1, nseg = *chi_flag - c_lo + 1;
+      merge_pieces(p.part_acc, p.part_ml, G, c_lo, nseg, outp, r, nthr);
+    }
+    named_bar_sync(bar_id, nthr);
+  };
 
   auto kslot = [&](int i) { return (2 * i) % p.stages; };
   auto kpar = [&](int i) { return (uint32_t)(((2 * i) / p.stages) & 1); };
@@ -489,6 +521,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       it_next(it, pre, B, Hkv);
     }
+  } else if (!KV8 && warp < 4) {
+    // ================================================================ piece publisher / merger
+    // bf16 cache: warps 2-3 take the cross-CTA step of every cut piece off
+    // the softmax group's path.  The group writes the piece's partial,
+    // arrives on pub_full[slot] (release at CTA scope) and goes on with the
+    // next piece; here the arrival is awaited (acquire), the pair's counter
+    // is bumped with an acquire-release atomic at GPU scope (which carries
+    // the group's partial stores with it), and the last piece's CTA merges.
+    // Each slot holds at most one piece per launch (slot 0: the share's
+    // first piece when it starts inside a pair; slot 1: a piece that starts
+    // a pair and is cut), so each barrier completes once, at parity 0.
+    const int ct = tid - 64;  // 0 .. 63
+    Iter it;
+    if (s_c < e_c) it_seek32(it, s_c, pre, B, Hkv);
+    int seg_lt0 = 0;
+    for (int t = s_c; t < e_c; ++t) {
+      if (t == s_c || it.lt == 0) seg_lt0 = it.lt;
+      const bool last = (t == e_c - 1) || it.lt == it.nb - 1;
+      if (last && !(seg_lt0 == 0 && it.lt == it.nb - 1)) {
+        mbar_wait_bounded(&pub_full[seg_lt0 == 0 ? 1 : 0], 0, abort_flag, p.err, p.wait_ns);
+        __nv_bfloat16* outp = p.out + ((size_t)it.b * p.Hq + (size_t)it.j * G) * kD;
+        publish_merge(it, outp, ct, 64, 2);
+      }
+      it_next(it, pre, B, Hkv);
+    }
   } else if (warp >= 4) {
     // ================================================================ softmax + epilogue
     const int r = tid - 128;                 // query head within the group = TMEM lane
@@ -664,29 +721,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_before_sync();
         if (!complete) {
-          // Publish the piece; the CTA that brings the pair's count to its
-          // number of pieces merges them all.
-          named_bar_sync(1, 128);
-          if (r == 0 && !*abort_flag) {
-            const int o_p = Hkv * pre[it.b] + it.j * it.nb;
-            const int c_lo = share_owner(sp, o_p);
-            const int c_hi = share_owner(sp, o_p + it.nb - 1);
-            const int pair = it.b * Hkv + it.j;
-            const int old = atomic_add_acq_rel_gpu(&p.counters[pair], 1);
-            const bool lastc = old == c_hi - c_lo;
-            if (lastc) p.counters[pair] = 0;  // ready for the next call (ordered by the kernel boundary)
-            *merge_flag = lastc ? c_lo + 1 : 0;
-            *chi_flag = c_hi;
-          } else if (r == 0) {
-            *merge_flag = 0;
+          if (KV8) {
+            publish_merge(it, outp, r, 128, 1);
+          } else {
+            // warps 2-3 count the piece in and merge; this group goes on
+            mbar_arrive(&pub_full[slot]);
           }
-          named_bar_sync(1, 128);
-          const int lf = *merge_flag;
-          if (lf) {
-            const int c_lo = lf - 1, nseg = *chi_flag - c_lo + 1;
-            merge_pieces(p.part_acc, p.part_ml, G, c_lo, nseg, outp, r);
-          }
-          named_bar_sync(1, 128);
         }
       }
       it_next(it, pre, B, Hkv);
