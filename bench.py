@@ -281,9 +281,13 @@ def bench_meanpool(g, W, dev, steps, warmup, flush, H=32, Hkv=8, D=128, d_model=
     return {"ms": ts, "bytes": (H + Hkv) * D * d_model * 2, "shape": (H, Hkv, D, d_model)}
 
 
-def bench_prefill(g, W, dev, steps, warmup, flush):
+def bench_prefill(g, W, dev, steps, warmup, flush, D=128):
+    """The causal prefill workload (B=4, L=2048, Hq=32, Hkv=8); D = 64 runs the
+    same shape at half the head size."""
     import torch
     w = W.WORKLOADS["prefill"]
+    if D != w.D:
+        w = W.PrefillWorkload(f"prefill_d{D}", w.B, w.L, w.Hq, w.Hkv, D, w.causal, w.seed)
     q, k, v = W.make_prefill_inputs(w)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     out = torch.empty_like(qd)
@@ -430,14 +434,14 @@ def run_reference(args, rank, world):
 
 def run_only(g, W, args, dev, flush, peaks):
     """One workload, for profiling and sweeps: prints the per-launch mean time and rate."""
-    if args.only == "prefill":
-        r = bench_prefill(g, W, dev, args.steps, args.warmup, flush)
+    if args.only in ("prefill", "prefill_d64"):
+        r = bench_prefill(g, W, dev, args.steps, args.warmup, flush, D=64 if args.only == "prefill_d64" else 128)
         if r is None:
-            print(json.dumps({"only": "prefill", "status": "not built"}))
+            print(json.dumps({"only": args.only, "status": "not built"}))
             return 0
         ms = statistics.mean(r["ms"])
         tf = r["flops"] / (ms / 1e3) / 1e12
-        print(json.dumps({"only": "prefill", "us": ms * 1e3, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]}))
+        print(json.dumps({"only": args.only, "us": ms * 1e3, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]}))
         return 0
     if args.only.endswith("_paged"):
         name = args.only[:-6]
@@ -479,7 +483,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="headline only (for profiling runs)")
     ap.add_argument("--only", default=None,
                     help="time one workload and print its line: a decode workload name (tiny, llama3_8b, "
-                         "llama2_70b, mqa), optionally with _fp8 or _paged; prefill; rope_append; kv_meanpool")
+                         "llama2_70b, mqa), optionally with _fp8 or _paged; prefill; prefill_d64; rope_append; kv_meanpool")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -571,6 +575,12 @@ def main():
                              "traffic": traffic_for(_csrc("prefill.cu"), "prefill")}}
         else:
             extras["prefill"] = {"status": "not built"}
+        p64 = bench_prefill(g, W, dev, small_steps, args.warmup, flush, D=64)
+        if p64 is not None:
+            pms = statistics.mean(p64["ms"])
+            tf = p64["flops"] / (pms / 1e3) / 1e12
+            extras["prefill_d64"] = {"workload": "causal prefill: B=4, L=2048, Hq=32, Hkv=8, D=64", "us": pms * 1e3,
+                                     "flops": p64["flops"], "TFLOP/s": tf, "frac_tensor": tf / peaks["bf16_tflops"]}
         pc = bench_prefill_chunk(g, W, dev, small_steps, args.warmup, flush)
         cms = statistics.mean(pc["ms"])
         ctf = pc["flops"] / (cms / 1e3) / 1e12

@@ -16,11 +16,15 @@
 // qb).  Each CTA is persistent and walks units heaviest first (causal units
 // with a large qb see the most keys) in a snake order over the grid.
 //
+// Head dimension D = 128 or 64 (a template parameter; rows of 128 or 64 bf16
+// are loaded as D / 64 boxes of 64 columns, 128 bytes per row).
+//
 // Warp roles (320 threads, one CTA per SM):
 //   warps 0-3  softmax of query tile 0 (thread = one query row = one TMEM lane)
 //   warps 4-7  softmax of query tile 1
 //   warp  8    TMA producer: the two Q tiles of a unit, then K/V blocks into a
-//              5-stage ring of 32 KiB slots (a slot holds one K or one V block)
+//              ring of slots of 128 x D bf16 (32 KiB at D = 128, 16 KiB at
+//              D = 64; 5 or 8 slots; a slot holds one K or one V block)
 //   warp  9    TMEM owner and tcgen05.mma issuer (the whole warp walks the
 //              schedule, one elected lane issues)
 //
@@ -36,7 +40,7 @@
 //                             the first 64 TMEM columns of S_t
 //   O_t += P_t V_j            TS MMA: A = P_t read from TMEM, B = V_j (smem,
 //                             MN-major), fp32 accumulator in TMEM columns
-//                             [256 + 128t, 256 + 128t + 128)
+//                             [256 + 128t, 256 + 128t + D)
 // The MMA warp interleaves the two tiles (S0, S1, PV0, S0', PV1, S1', ...),
 // so that the tensor pipe works on one tile while the other tile's softmax
 // runs.  TMEM: S0, S1, O0, O1 = 512 columns.  At the end of a unit each
@@ -58,25 +62,27 @@
 namespace gqa {
 namespace {
 
-constexpr int kD = 128;          // head dim
 constexpr int kBM = 128;         // query rows per tile
 constexpr int kBN = 128;         // keys per block
-constexpr int kStages = 5;       // K/V ring depth (a slot holds one K or one V block)
-constexpr int kTileBytes = kBM * kD * 2;  // 32 KiB: one Q tile, P tile, K or V block
-constexpr int kHalfBytes = kTileBytes / 2;  // one 64-column half (128-byte rows)
+constexpr int kBoxBytes = kBM * 128;  // one 64-column box of a tile (128-byte rows): 16 KiB
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRebaseLog2 = 8.0f;  // re-base the running max when it grows by more
 
-// Shared memory (offsets from a 1024-byte aligned base).
-constexpr int kOffQ = 0;                              // 2 query tiles
-constexpr int kOffRing = kOffQ + 2 * kTileBytes;      // kStages K/V blocks
-constexpr int kOffBars = kOffRing + kStages * kTileBytes;
-constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 1;
-constexpr int kOffMisc = kOffBars + kNumBars * 8;     // TMEM base, abort flag
-constexpr size_t kSmemBytes = (size_t)kOffMisc + 16 + 1024;  // + alignment slack
+// Shared memory of the D instantiation (offsets from a 1024-byte aligned base).
+template <int D>
+struct Cfg {
+  static constexpr int kTileBytes = kBM * D * 2;  // one Q tile, K or V block
+  static constexpr int kStages = D == 64 ? 8 : 5;  // K/V ring depth (a slot holds one K or one V block)
+  static constexpr int kOffQ = 0;                  // 2 query tiles
+  static constexpr int kOffRing = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffBars = kOffRing + kStages * kTileBytes;
+  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 1;
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;  // TMEM base, abort flag
+  static constexpr size_t kSmemBytes = (size_t)kOffMisc + 16 + 1024;  // + alignment slack
+};
 
 struct Params {
   __nv_bfloat16* out;
@@ -132,9 +138,13 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using C = Cfg<D>;
+  constexpr int kTileBytes = C::kTileBytes, kStages = C::kStages;
+  constexpr int kOffQ = C::kOffQ, kOffRing = C::kOffRing, kOffBars = C::kOffBars, kOffMisc = C::kOffMisc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
@@ -198,8 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* dst = smem + kOffQ + t * kTileBytes;
           mbar_arrive_expect_tx(&q_full[t], kTileBytes);
           const int row = x.b * p.Hq + x.h0 + t;
-          tma_load_3d(dst, &tm_q, 0, x.qb * kBM, row, &q_full[t], pol_q);
-          tma_load_3d(dst + kHalfBytes, &tm_q, 64, x.qb * kBM, row, &q_full[t], pol_q);
+#pragma unroll
+          for (int box = 0; box < D / 64; ++box)
+            tma_load_3d(dst + box * kBoxBytes, &tm_q, box * 64, x.qb * kBM, row, &q_full[t], pol_q);
           q_used = i + 1;
         }
         const int kvrow = x.b * p.Hkv + x.j;
@@ -212,8 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* dst = smem + kOffRing + s * kTileBytes;
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
             mbar_arrive_expect_tx(&kv_full[s], kTileBytes);
-            tma_load_3d(dst, m, 0, jb * kBN, kvrow, &kv_full[s], pol_kv);
-            tma_load_3d(dst + kHalfBytes, m, 64, jb * kBN, kvrow, &kv_full[s], pol_kv);
+#pragma unroll
+            for (int box = 0; box < D / 64; ++box)
+              tma_load_3d(dst + box * kBoxBytes, m, box * 64, jb * kBN, kvrow, &kv_full[s], pol_kv);
             slot_used |= 1u << s;
             slot_par = (slot_par & ~(1u << s)) | (par << s);
             ++kv_it;
@@ -232,20 +244,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every descriptor is a warp-uniform value; one elected lane issues the
     // MMAs and the commits that track them.
     constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false);
-    constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kBM, kD, true);
+    constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kBM, D, true);
     const bool leader = elect_one_sync();
     // Descriptors of the tile bases; the address field (bits 0-13, in 16-byte
     // units) is advanced by adding the byte offset >> 4 (no carry: smem < 256 KiB).
     const uint64_t dq = tc::sdesc_sw128(smem_u32(smem + kOffQ), 16, 1024);
     const uint64_t dk = tc::sdesc_sw128(smem_u32(smem + kOffRing), 16, 1024);
-    const uint64_t dv = tc::sdesc_sw128(smem_u32(smem + kOffRing), kHalfBytes, 1024);
+    // (the leading-byte offset steps between 64-column boxes along N = D)
+    const uint64_t dv = tc::sdesc_sw128(smem_u32(smem + kOffRing), kBoxBytes, 1024);
     auto issue_s = [&](int t, int slot) {
       const uint64_t a0 = dq + (uint64_t)((t * kTileBytes) >> 4);
       const uint64_t b0 = dk + (uint64_t)((slot * kTileBytes) >> 4);
       if (leader) {
 #pragma unroll
-        for (int k = 0; k < kD / 16; ++k) {
-          const uint64_t off = (uint64_t)(((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4);
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t off = (uint64_t)(((k >> 2) * kBoxBytes + (k & 3) * 32) >> 4);
           tc::mma_ss(tmem + t * 128, a0 + off, b0 + off, idesc_s, k > 0);
         }
       }
@@ -424,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // also covered the previous P V); bring it to the new reference.
         if (any_rebase && jb > 0) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tc::ld_32x32b_x32(o_tm + c * 32, o);
             tc::wait_ld_regs(o);
@@ -444,9 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++oc;
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.out + ((size_t)(x.b * p.Hq + h) * p.Lq + qi) * kD;
+      __nv_bfloat16* orow = p.out + ((size_t)(x.b * p.Hq + h) * p.Lq + qi) * D;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tc::ld_32x32b_x32(o_tm + c * 32, o);
         tc::wait_ld_regs(o);
@@ -476,10 +489,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-bool prefill_supported(int D) { return D == kD; }
+bool prefill_supported(int D) { return D == 64 || D == 128; }
+
+template <int D>
+cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const Params& p, int grid,
+                     cudaStream_t stream) {
+  static std::atomic<unsigned long long> attr_set{0};  // one bit per device ordinal < 64
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !(attr_set.load() >> dev & 1ull)) {
+    e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set.fetch_or(1ull << dev);
+  }
+  prefill_kernel<D><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
 
 cudaError_t prefill_launch(const PrefillArgs& a, int sm_count, cudaStream_t stream) {
-  if (a.D != kD) return cudaErrorNotSupported;
+  if (!prefill_supported(a.D)) return cudaErrorNotSupported;
   const int Lk = a.Lk > 0 ? a.Lk : a.L;
   if (Lk < a.L) return cudaErrorInvalidValue;
   const uint64_t rowb = (uint64_t)a.D * 2, qheadb = (uint64_t)a.L * a.D * 2, kheadb = (uint64_t)Lk * a.D * 2;
@@ -509,18 +538,8 @@ cudaError_t prefill_launch(const PrefillArgs& a, int sm_count, cudaStream_t stre
   p.err = a.err;
   p.wait_ns = pipeline_wait_limit_ns();
   p.starve = pipeline_starved() ? 1 : 0;
-  static std::atomic<unsigned long long> attr_set{0};  // one bit per device ordinal < 64
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(attr_set.load() >> dev & 1ull)) {
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set.fetch_or(1ull << dev);
-  }
   const int grid = (int)std::min<long long>(units, sm_count);
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  return a.D == 64 ? launch_d<64>(tq, tk, tv, p, grid, stream) : launch_d<128>(tq, tk, tv, p, grid, stream);
 }
 
 }  // namespace gqa

@@ -143,7 +143,8 @@ GQA_API int gqa_decode_fp8(const void* q, const void* k_cache, const void* v_cac
  * fp32 accumulators in tensor memory; the softmax is fp32; P is rounded to
  * bf16 before PV; out is rounded RNE.
  *
- * Supported: D == 128, any L >= 1, any G.  Otherwise GQA_ERR_UNSUPPORTED.
+ * Supported: D == 128 or D == 64, any L >= 1, any G.  Otherwise
+ * GQA_ERR_UNSUPPORTED.
  * Needs no workspace and allocates nothing.
  */
 GQA_API int gqa_prefill(const void* q, const void* k, const void* v, void* out, int B, int L, int Hq,
@@ -217,7 +218,7 @@ GQA_API int gqa_rope_append(const void* q, const void* k_new, const void* v_new,
  *   q, out   [B, Hq, Lq, D]   bf16, device
  *   k, v     [B, Hkv, Lk, D]  bf16, device (Lk >= Lq)
  *
- * Same kernel, arithmetic, scale (1/sqrt(D)) and support (D == 128) as
+ * Same kernel, arithmetic, scale (1/sqrt(D)) and support (D == 64 or 128) as
  * gqa_prefill.  Allocates nothing.
  */
 GQA_API int gqa_prefill_chunk(const void* q, const void* k, const void* v, void* out, int B, int Lq, int Lk,

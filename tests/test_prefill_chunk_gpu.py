@@ -9,11 +9,11 @@ from parity import assert_parity
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(B, Hq, Hkv, Lq, Lk, seed):
+def _inputs(B, Hq, Hkv, Lq, Lk, seed, D=128):
     g = torch.Generator().manual_seed(seed)
-    q = torch.randn(B, Hq, Lq, 128, generator=g).to(torch.bfloat16)
-    k = torch.randn(B, Hkv, Lk, 128, generator=g).to(torch.bfloat16)
-    v = torch.randn(B, Hkv, Lk, 128, generator=g).to(torch.bfloat16)
+    q = torch.randn(B, Hq, Lq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Hkv, Lk, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Hkv, Lk, D, generator=g).to(torch.bfloat16)
     return q, k, v
 
 
@@ -32,6 +32,20 @@ def test_chunk_parity(gqa_lib, oracle_mod, cuda_device, B, Hq, Hkv, Lq, Lk, caus
     assert gqa_lib.gqa_get_device_status() == 0
     ref = oracle_mod.prefill_chunk(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), causal=causal)
     assert_parity(out.double().cpu().numpy(), ref, f"chunk {B},{Hq},{Hkv},{Lq},{Lk},{causal}")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,causal", [
+    (2, 8, 2, 300, 1000, True),    # ragged chunk after a 700-token prefix
+    (1, 8, 1, 1, 129, True),       # one token
+    (2, 6, 2, 200, 333, False),    # full attention over prefix + chunk
+])
+def test_chunk_d64_parity(gqa_lib, oracle_mod, cuda_device, B, Hq, Hkv, Lq, Lk, causal):
+    q, k, v = _inputs(B, Hq, Hkv, Lq, Lk, 6300 + Lq + Lk, D=64)
+    d = cuda_device
+    out = gqa_lib.gqa_prefill_chunk(q.to(d), k.to(d), v.to(d), causal=causal)
+    assert gqa_lib.gqa_get_device_status() == 0
+    ref = oracle_mod.prefill_chunk(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), causal=causal)
+    assert_parity(out.double().cpu().numpy(), ref, f"chunk D=64 {B},{Hq},{Hkv},{Lq},{Lk},{causal}")
 
 
 def test_chunk_full_size_every_element(gqa_lib, oracle_mod, cuda_device):

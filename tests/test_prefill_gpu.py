@@ -48,6 +48,44 @@ def test_shapes_parity(gqa_lib, oracle_mod, cuda_device, B, Hq, Hkv, L, causal):
     assert_parity(out.double().numpy(), ref, f"{B},{Hq},{Hkv},{L},{causal}")
 
 
+# ---- D = 64 (the head size d_model / num_heads of the Huawei Cloud post,
+# section 5, is not fixed at 128): 16 KiB tiles and blocks, one 64-column
+# box per row, an 8-slot ring, PV with N = 64.
+@pytest.mark.parametrize("B,Hq,Hkv,L,causal", [
+    (1, 2, 1, 128, True),      # one unit, one diagonal block
+    (1, 4, 2, 300, True),      # ragged last tile, three query tiles
+    (2, 8, 2, 129, False),     # full attention, ragged last key block
+    (1, 3, 1, 200, True),      # odd G: one head per unit
+    (1, 8, 1, 1, True),        # a single token
+    (1, 32, 4, 640, True),     # G = 8
+    (4, 16, 4, 1152, True),    # 288 units: every CTA walks two of them
+])
+def test_d64_shapes_parity(gqa_lib, oracle_mod, cuda_device, B, Hq, Hkv, L, causal):
+    w = W.PrefillWorkload("case64", B, L, Hq, Hkv, 64, causal, 700 + B * Hq + L)
+    q, k, v = W.make_prefill_inputs(w)
+    out, flags = run_prefill(gqa_lib, q, k, v, causal, cuda_device)
+    assert flags == 0
+    ref = oracle_prefill(oracle_mod, q, k, v, causal)
+    assert_parity(out.double().numpy(), ref, f"D=64 {B},{Hq},{Hkv},{L},{causal}")
+
+
+def test_d64_peaky_and_full_size(gqa_lib, oracle_mod, cuda_device):
+    """D = 64 with q x 8 (re-based running max), then every element of a
+    causal B=4, L=2048, Hq=32, Hkv=8 prompt (the benchmark's prefill shape at
+    half the head size)."""
+    w = W.PrefillWorkload("peaky64", 2, 768, 8, 2, 64, True, 72)
+    q, k, v = W.make_prefill_inputs(w, q_mult=8.0)
+    for causal in (True, False):
+        out, flags = run_prefill(gqa_lib, q, k, v, causal, cuda_device)
+        assert flags == 0
+        assert_parity(out.double().numpy(), oracle_prefill(oracle_mod, q, k, v, causal), f"D=64 peaky {causal}")
+    w = W.PrefillWorkload("full64", 4, 2048, 32, 8, 64, True, 73)
+    q, k, v = W.make_prefill_inputs(w)
+    out, flags = run_prefill(gqa_lib, q, k, v, True, cuda_device)
+    assert flags == 0
+    assert_parity(out.double().numpy(), oracle_prefill(oracle_mod, q, k, v, True), "D=64 full size")
+
+
 def test_peaky_softmax_rebases_running_max(gqa_lib, oracle_mod, cuda_device):
     """q x 8: logits with a spread of tens, so the running max of a row grows
     by more than the re-base margin from block to block and the rescale of the
