@@ -148,6 +148,39 @@ __device__ inline int cta_of(long long t, long long T, int P) {
 
 __device__ inline int clamp_len(int len, int Lmax) { return len < 0 ? 0 : (len > Lmax ? Lmax : len); }
 
+// E4M3 tiles (rows of D bytes, as TMA lands them): the 16-byte chunk c of row
+// r sits at chunk c ^ (r & 7) with D = 128 (128-byte swizzle) and at
+// c ^ ((r >> 1) & 3) with D = 64 (64-byte swizzle; a 128-byte line holds two
+// rows).  Rows r and r + 8 share the pattern in both.
+template <int D>
+__device__ __forceinline__ int e4m3_chunk(int c, int r) {
+  return D == 128 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3));
+}
+
+// V bytes a lane takes from one row of an E4M3 tile: 16 bytes (d = 16 g ..
+// 16 g + 15) at D = 128, 8 bytes (d = 8 g .. 8 g + 7) at D = 64 -- the output
+// rows of the lane's m-rows g and g + 8 (see the PV product).
+template <int D>
+struct V8Frag {
+  uint32_t w[D / 32];
+};
+template <int D>
+__device__ __forceinline__ V8Frag<D> load_v8(const uint8_t* tile, int row, int g) {
+  V8Frag<D> f;
+  if constexpr (D == 128) {
+    const uint4 x = *reinterpret_cast<const uint4*>(tile + row * 128 + (e4m3_chunk<128>(g, row) << 4));
+    f.w[0] = x.x;
+    f.w[1] = x.y;
+    f.w[2] = x.z;
+    f.w[3] = x.w;
+  } else {
+    const uint2 x = *reinterpret_cast<const uint2*>(tile + row * 64 + (e4m3_chunk<64>(g >> 1, row) << 4) + 8 * (g & 1));
+    f.w[0] = x.x;
+    f.w[1] = x.y;
+  }
+  return f;
+}
+
 // Consumer warp groups per CTA: with one n-tile per warp (G <= 8) a single
 // group leaves one consumer warp per SM sub-partition, whose per-tile
 // dependency chain then sets the pace; two groups on alternate tiles overlap
@@ -162,7 +195,7 @@ __global__ void __launch_bounds__(288, 1)
   constexpr int KT = D / 16;  // 16-wide k-steps over D (QK) and m-tiles over D (PV)
   constexpr int NG = tile_groups<NT>();
   constexpr int KS = kKW * NG;  // key-slice states merged at the end of a piece
-  static_assert(!KV8 || (D == 128 && NT == 1), "the FP8 cache path is built for D = 128, G <= 8");
+  static_assert(!KV8 || NT == 1, "the FP8 cache path is built for G <= 8");
   const int Gpad = p.HS * 8 * NT;
   const SmemLayout L = smem_layout<D>(p.stages, Gpad, NG, KV8, p.G);
   // Each tile group has a private ring of SG stages: tile i belongs to group
@@ -484,15 +517,16 @@ __global__ void __launch_bounds__(288, 1)
         //     rows d undone when the accumulators are stored.
         //   V rows at or past seqlens[b] read as zeros (the cache may hold
         //   anything there, NaN included).
-        uint4 k8[2][2], v8[4];
+        uint4 k8[D / 64][2];
+        V8Frag<D> v8[4];
         if constexpr (KV8) {
           const uint8_t* kt = smem + s * L.stage_bytes;
           const int g = key0 + (lane >> 2);
 #pragma unroll
-          for (int hd = 0; hd < 2; ++hd) {
-            const int ch = ((4 * hd + (lane & 3)) ^ (g & 7)) << 4;  // rows g and g + 8 share g & 7
-            k8[hd][0] = *reinterpret_cast<const uint4*>(kt + g * 128 + ch);
-            k8[hd][1] = *reinterpret_cast<const uint4*>(kt + (g + 8) * 128 + ch);
+          for (int hd = 0; hd < D / 64; ++hd) {
+            const int ch = e4m3_chunk<D>(4 * hd + (lane & 3), g) << 4;  // rows g and g + 8 share the swizzle
+            k8[hd][0] = *reinterpret_cast<const uint4*>(kt + g * D + ch);
+            k8[hd][1] = *reinterpret_cast<const uint4*>(kt + (g + 8) * D + ch);
           }
         } else if (valid < key0 + 16) {
           // Rows past the sequence end hold whatever the cache holds there
@@ -622,8 +656,7 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int row = key0 + 2 * (lane & 3) + (r & 1) + 8 * (r >> 1);
-            v8[r] = row < valid ? *reinterpret_cast<const uint4*>(vt + row * 128 + (((lane >> 2) ^ (row & 7)) << 4))
-                                : make_uint4(0, 0, 0, 0);
+            v8[r] = row < valid ? load_v8<D>(vt, row, lane >> 2) : V8Frag<D>{};
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
@@ -637,10 +670,7 @@ __global__ void __launch_bounds__(288, 1)
             // 2 mt (m-row g) and 2 mt + 1 (m-row g + 8)
             const int w = mt >> 1;
             const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-            const uint32_t r0 = w == 0 ? v8[0].x : w == 1 ? v8[0].y : w == 2 ? v8[0].z : v8[0].w;
-            const uint32_t r1 = w == 0 ? v8[1].x : w == 1 ? v8[1].y : w == 2 ? v8[1].z : v8[1].w;
-            const uint32_t r8 = w == 0 ? v8[2].x : w == 1 ? v8[2].y : w == 2 ? v8[2].z : v8[2].w;
-            const uint32_t r9 = w == 0 ? v8[3].x : w == 1 ? v8[3].y : w == 2 ? v8[3].z : v8[3].w;
+            const uint32_t r0 = v8[0].w[w], r1 = v8[1].w[w], r8 = v8[2].w[w], r9 = v8[3].w[w];
             e4m3x4_to_f16x2x2(__byte_perm(r0, r1, sel), a[0], a[1]);
             e4m3x4_to_f16x2x2(__byte_perm(r8, r9, sel), a[2], a[3]);
           } else {
@@ -682,9 +712,9 @@ __global__ void __launch_bounds__(288, 1)
             float* e0 = epi + (size_t)(slice * G + hg) * (D + 4);  // rows of padding heads are not kept
             float* e1 = e0 + (D + 4);
             if constexpr (KV8) {
-              // m-rows g, g + 8 of m-tile mt are d = 16 g + 2 mt and + 1; the
-              // FP8 cache's V scale is applied here, once per piece
-              const int d = 16 * (lane >> 2) + 2 * mt;
+              // m-rows g, g + 8 of m-tile mt are d = (D / 8) g + 2 mt and + 1;
+              // the FP8 cache's V scale is applied here, once per piece
+              const int d = (D / 8) * (lane >> 2) + 2 * mt;
               if (hg < G)
                 *reinterpret_cast<float2*>(e0 + d) = make_float2(acc[mt][nt][0] * v_mul, acc[mt][nt][2] * v_mul);
               if (hg + 1 < G)
@@ -900,7 +930,7 @@ cudaError_t cache_tensor_maps(const DecodeArgs& a, int D, bool kv8, CUtensorMap*
   n.kv8 = (int)kv8;
   n.pairs = pairs;
   if (kv8) {
-    // E4M3 bytes: one 128-byte box covers a row of D = 128 elements
+    // E4M3 bytes: one box of D bytes covers a row (128- or 64-byte swizzle)
     const uint64_t s1 = (uint64_t)D, s2 = (uint64_t)rows * D;
     if (encode_tmap_u8_3d(&n.tk, a.k_cache, D, rows, pairs, s1, s2, D, kBN, 1) != CUDA_SUCCESS ||
         encode_tmap_u8_3d(&n.tv, a.v_cache, D, rows, pairs, s1, s2, D, kBN, 1) != CUDA_SUCCESS)
@@ -976,8 +1006,8 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
   if (B < 1 || B > kMaxBatch || Hkv < 1 || Hq % Hkv != 0 || Lmax < 1) return false;
   if (D != 64 && D != 128) return false;
   const int G = Hq / Hkv;
-  // An FP8 cache is built for D = 128.
-  if (kv8 && D != 128) return false;
+  // An FP8 cache: D = 128 (every G <= 128) or D = 64 (G <= 8).
+  if (kv8 && D == 64 && G > 8) return false;
   // Wide groups at D = 128 go to the tcgen05 kernel: its tensor core reads
   // each K/V block from shared memory once for all G heads.
   if (D == 128 && G > 8 && G <= 128) {
@@ -1036,8 +1066,8 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
 cudaError_t decode_launch(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t stream) {
   if (plan.kind == 1) return decode_tc_launch(plan, a, stream);
   if (plan.kv8) {
-    if (plan.D != 128 || plan.NT != 1 || !a.k_scale || !a.v_scale) return cudaErrorInvalidValue;
-    return launch_t<128, 1, true>(plan, a, stream);
+    if (plan.NT != 1 || !a.k_scale || !a.v_scale) return cudaErrorInvalidValue;
+    return plan.D == 128 ? launch_t<128, 1, true>(plan, a, stream) : launch_t<64, 1, true>(plan, a, stream);
   }
   if (plan.D == 128) {
     // groups wider than 8 at D = 128 run on the tcgen05 kernel (decode_plan)

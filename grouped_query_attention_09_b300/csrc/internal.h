@@ -29,7 +29,8 @@ cudaError_t noalloc_take_status(unsigned* flags);
 CUresult encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1,
                              uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
                              uint32_t box1, uint32_t box2);
-// The same for a byte tensor (FP8 cache stored as uint8).
+// The same for a byte tensor (FP8 cache stored as uint8); a 64-byte inner box
+// takes the 64-byte swizzle instead.
 CUresult encode_tmap_u8_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
                            uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2);
 

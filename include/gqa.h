@@ -118,11 +118,12 @@ GQA_API int gqa_decode(const void* q, const void* k_cache, const void* v_cache, 
  * the logit scale and the V scale the output.  Cache rows at or beyond
  * seqlens[b] are never used (they may hold anything, NaN bytes included).
  *
- * Supported: D == 128, 1 <= G = Hq/Hkv <= 128, 1 <= B <= 1024.  Otherwise
- * GQA_ERR_UNSUPPORTED.  G <= 8 runs the warp-level kernel (E4M3 bytes
- * converted in registers); wider groups run the tcgen05 kernel, whose
- * converter warps turn each E4M3 block into fp16 in shared memory for fp16
- * MMAs.  Workspace, streams and device status as gqa_decode.
+ * Supported: D == 128 with 1 <= G = Hq/Hkv <= 128, or D == 64 with G <= 8;
+ * 1 <= B <= 1024.  Otherwise GQA_ERR_UNSUPPORTED.  G <= 8 runs the
+ * warp-level kernel (E4M3 bytes converted in registers); wider groups run the
+ * tcgen05 kernel, whose converter warps turn each E4M3 block into fp16 in
+ * shared memory for fp16 MMAs.  Workspace, streams and device status as
+ * gqa_decode.
  */
 GQA_API int gqa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
                            const float* v_scale, const int32_t* seqlens, void* out, int B, int Hq, int Hkv,

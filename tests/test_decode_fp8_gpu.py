@@ -113,11 +113,47 @@ def test_fp8_wide_group_nan_tail_and_edges(gqa_lib, oracle_mod, cuda_device):
     assert_parity(out[keep], ref[keep], "fp8 wide edges")
 
 
-def test_fp8_rejects_d64(gqa_lib, cuda_device):
-    w = W.DecodeWorkload("fp8_d64", 2, 8, 2, 64, 128, 1, 128, 102)
-    q = torch.zeros(2, 8, 64, dtype=torch.bfloat16, device=cuda_device)
-    k8 = torch.zeros(2, 2, 128, 64, dtype=torch.uint8, device=cuda_device)
-    sc = torch.ones(2, 2, device=cuda_device)
+# ---- D = 64: rows of 64 E4M3 bytes (64-byte swizzle), G <= 8
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,lens", [
+    (2, 8, 2, 128, [128, 77]),            # the tiny decode shape
+    (3, 8, 2, 700, [700, 333, 65]),       # ragged tails, many tiles
+    (4, 4, 4, 257, [63, 64, 65, 257]),    # MHA endpoint; tile boundaries
+    (2, 6, 2, 300, [300, 17]),            # G = 3
+    (16, 32, 8, 2048, [2048] * 16),       # one CTA per pair, L2 prefetch at launch
+])
+def test_fp8_d64_shapes(gqa_lib, oracle_mod, cuda_device, B, Hq, Hkv, Lmax, lens):
+    w = W.DecodeWorkload("fp8_d64", B, Hq, Hkv, 64, Lmax, 1, Lmax, 3100 + B * Hq + Lmax)
+    q, k8, v8, ks, vs, _ = W.make_decode_fp8_inputs(w)
+    sl = torch.tensor(lens, dtype=torch.int32)
+    out, flags = run_fp8(gqa_lib, q, k8, v8, ks, vs, sl, w.scale, cuda_device)
+    assert flags == 0
+    assert_parity(out, oracle_fp8(oracle_mod, q, k8, v8, ks, vs, sl, w.scale), f"fp8 D=64 {B},{Hq},{Hkv},{lens}")
+
+
+def test_fp8_d64_nan_tail_and_edges(gqa_lib, oracle_mod, cuda_device):
+    """D = 64: E4M3 NaN bytes past every sequence end, q x 8, an empty
+    context and a clamped length in one batch."""
+    w = W.DecodeWorkload("fp8_d64_edges", 5, 16, 4, 64, 1024, 1, 1024, 98)
+    sl = torch.tensor([1024, 1, 700, 0, 9999], dtype=torch.int32)
+    q, k8, v8, ks, vs, _ = W.make_decode_fp8_inputs(w, q_mult=8.0)
+    for b in range(5):
+        n = int(sl[b].clamp(0, 1024))
+        k8[b, :, n:, :] = W.E4M3_NAN
+        v8[b, :, n:, :] = W.E4M3_NAN
+    out, flags = run_fp8(gqa_lib, q, k8, v8, ks, vs, sl, w.scale, cuda_device)
+    assert flags == (gqa_lib.GQA_DEV_EMPTY_CONTEXT | gqa_lib.GQA_DEV_SEQLEN_CLAMPED)
+    assert np.all(out[3] == 0)
+    ref = oracle_fp8(oracle_mod, q, k8, v8, ks, vs, sl.clamp(min=1, max=1024), w.scale)
+    keep = [0, 1, 2, 4]
+    assert_parity(out[keep], ref[keep], "fp8 D=64 edges")
+
+
+def test_fp8_rejects_d64_wide_groups(gqa_lib, cuda_device):
+    """D = 64 with 16 heads per KV head has no FP8 kernel."""
+    w = W.DecodeWorkload("fp8_d64_g16", 2, 16, 1, 64, 128, 1, 128, 102)
+    q = torch.zeros(2, 16, 64, dtype=torch.bfloat16, device=cuda_device)
+    k8 = torch.zeros(2, 1, 128, 64, dtype=torch.uint8, device=cuda_device)
+    sc = torch.ones(2, 1, device=cuda_device)
     sl = torch.full((2,), 128, dtype=torch.int32, device=cuda_device)
     with pytest.raises(gqa_lib.GQAError) as e:
         gqa_lib.gqa_decode_fp8(q, k8, k8, sc, sc, sl, scale=w.scale)
