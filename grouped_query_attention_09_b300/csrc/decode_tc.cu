@@ -468,23 +468,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t == s_c || it.lt == 0) {
         // The pair's query heads as fp16 rows of the Q tile (128-byte swizzle,
         // two 64-column halves), once the previous piece's scores are done.
+        // Eight 16-byte pieces of q per thread are loaded at once (all of
+        // them for G <= 32, before the wait), so the global-load latency is
+        // paid once per batch, not once per piece.
+        const __nv_bfloat16* qb = p.q + ((size_t)it.b * p.Hq + (size_t)it.j * G) * kD;
+        const int nq = G * 16;  // 16-byte pieces of the group's q
+        uint4 x[8];
+        auto load_q = [&](int e0) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int e = e0 + ct + u * kConv;
+            x[u] = e < nq ? __ldg(reinterpret_cast<const uint4*>(qb + (size_t)(e >> 4) * kD + (e & 15) * 8))
+                          : make_uint4(0, 0, 0, 0);
+          }
+        };
+        auto store_q = [&](int e0) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int e = e0 + ct + u * kConv, row = e >> 4, c16 = e & 15;
+            if (e < nq) {
+              const uint4 h = make_uint4(
+                  pack_f16x2(__uint_as_float(x[u].x << 16), __uint_as_float(x[u].x & 0xFFFF0000u)),
+                  pack_f16x2(__uint_as_float(x[u].y << 16), __uint_as_float(x[u].y & 0xFFFF0000u)),
+                  pack_f16x2(__uint_as_float(x[u].z << 16), __uint_as_float(x[u].z & 0xFFFF0000u)),
+                  pack_f16x2(__uint_as_float(x[u].w << 16), __uint_as_float(x[u].w & 0xFFFF0000u)));
+              *reinterpret_cast<uint4*>(q_tile + (c16 >> 3) * kHalf + row * 128 + (((c16 & 7) ^ (row & 7)) << 4)) = h;
+            }
+          }
+        };
+        load_q(0);
+        const int seq_len = __ldg(p.seqlens + it.b);
         ok = mbar_wait_bounded(q_empty, (seg & 1) ^ 1, abort_flag, p.err, p.wait_ns);
         if (!ok) break;
-        const __nv_bfloat16* qb = p.q + ((size_t)it.b * p.Hq + (size_t)it.j * G) * kD;
-        for (int e = ct; e < G * 16; e += kConv) {
-          const int row = e >> 4, c16 = e & 15;
-          const uint4 x = __ldg(reinterpret_cast<const uint4*>(qb + (size_t)row * kD + c16 * 8));
-          const uint4 h = make_uint4(
-              pack_f16x2(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xFFFF0000u)),
-              pack_f16x2(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xFFFF0000u)),
-              pack_f16x2(__uint_as_float(x.z << 16), __uint_as_float(x.z & 0xFFFF0000u)),
-              pack_f16x2(__uint_as_float(x.w << 16), __uint_as_float(x.w & 0xFFFF0000u)));
-          *reinterpret_cast<uint4*>(q_tile + (c16 >> 3) * kHalf + row * 128 + (((c16 & 7) ^ (row & 7)) << 4)) = h;
+        store_q(0);
+        for (int e0 = 8 * kConv; e0 < nq; e0 += 8 * kConv) {
+          load_q(e0);
+          store_q(e0);
         }
         fence_proxy_async_smem();
         mbar_arrive(q_full);
         ++seg;
-        len_b = clamp_seq(p.seqlens[it.b], p.Lmax);
+        len_b = clamp_seq(seq_len, p.Lmax);
       }
       const int valid = min(kBN, len_b - it.lt * kBN);
       for (int kv = 0; kv < 2 && ok; ++kv) {
@@ -496,24 +520,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 16 E4M3 bytes (d = 16c .. 16c + 15 of row r) become two 16-byte
         // fp16 chunks of the row's half c / 4.  V rows at and past the
         // sequence end become zeros (the cache may hold NaN bytes there).
+        // Thread ct takes chunk c = ct % 8 of rows ct / 8 + 8u (u < 16), all
+        // in the same swizzle phase; the 16 loads go out before any
+        // conversion, and the row test selects after it (no branch).
         const uint8_t* src = ring8 + s8 * kBlockBytes8;
         uint8_t* dst = ring + s * kBlockBytes;
         const int zero_from = kv ? valid : kBN;
-#pragma unroll 4
-        for (int e = ct; e < kBN * 8; e += kConv) {
-          const int r = e >> 3, c = e & 7;
-          uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-          if (r < zero_from) {
-            const uint4 w = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
-            e4m3x4_to_f16x2x2(w.x, lo.x, lo.y);
-            e4m3x4_to_f16x2x2(w.y, lo.z, lo.w);
-            e4m3x4_to_f16x2x2(w.z, hi.x, hi.y);
-            e4m3x4_to_f16x2x2(w.w, hi.z, hi.w);
-          }
-          uint8_t* row = dst + (c >> 2) * kHalf + r * 128;
-          const int cc = 2 * (c & 3);
-          *reinterpret_cast<uint4*>(row + ((cc ^ (r & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (r & 7)) << 4)) = hi;
+        constexpr int kIt = kBN * 8 / kConv;
+        const int c = ct & 7, r0 = ct >> 3, sw = r0 & 7;
+        uint4 wv[kIt];
+#pragma unroll
+        for (int u = 0; u < kIt; ++u)
+          wv[u] = *reinterpret_cast<const uint4*>(src + (r0 + 8 * u) * 128 + ((c ^ sw) << 4));
+        const int cc = 2 * (c & 3);
+        uint8_t* base = dst + (c >> 2) * kHalf + r0 * 128;
+#pragma unroll
+        for (int u = 0; u < kIt; ++u) {
+          uint4 lo, hi;
+          e4m3x4_to_f16x2x2(wv[u].x, lo.x, lo.y);
+          e4m3x4_to_f16x2x2(wv[u].y, lo.z, lo.w);
+          e4m3x4_to_f16x2x2(wv[u].z, hi.x, hi.y);
+          e4m3x4_to_f16x2x2(wv[u].w, hi.z, hi.w);
+          if (r0 + 8 * u >= zero_from) lo = hi = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(base + u * 1024 + ((cc ^ sw) << 4)) = lo;
+          *reinterpret_cast<uint4*>(base + u * 1024 + (((cc + 1) ^ sw) << 4)) = hi;
         }
         fence_proxy_async_smem();
         mbar_arrive(&e8_empty[s8]);
