@@ -127,9 +127,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_done = p_full + 2;
   uint64_t* o_full = o_done + 1;
   uint64_t* mma_done = o_full + 1;
-  uint64_t* e8_full = mma_done + 1;   // [S8] an E4M3 block landed (KV8)
-  uint64_t* e8_empty = e8_full + S8;  // [S8] ... and was converted (KV8)
-  uint64_t* pub_full = e8_empty + S8;  // [2] partial slot 0 / 1 written (bf16 cache: merged by warps 2-3)
+  // (The E4M3 ring's barriers exist only with KV8: tc_layout reserves 2 S8
+  // of them then and none for a bf16 cache, so the pointers step by 0 there.)
+  const int S8b = KV8 ? p.stages8 : 0;
+  uint64_t* e8_full = mma_done + 1;    // [S8] an E4M3 block landed (KV8)
+  uint64_t* e8_empty = e8_full + S8b;  // [S8] ... and was converted (KV8)
+  uint64_t* pub_full = e8_empty + S8b;  // [2] partial slot 0 / 1 written (bf16 cache: merged by warps 2-3)
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
   volatile int* abort_flag = misc;
   volatile int* merge_flag = misc + 1;

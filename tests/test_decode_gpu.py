@@ -163,9 +163,8 @@ def test_side_stream_and_host_entry_point(gqa_lib, cuda_device):
     assert torch.equal(ref.cpu(), host)
 
 
-# ---- wide groups (G > 8 at D = 128): the tcgen05 decode kernels, keys as
-# the MMA rows for G <= 32 (16 or 32 padded head columns), heads as the MMA
-# rows above
+# ---- wide groups (G > 8 at D = 128): the tcgen05 decode kernel, the
+# group's heads as the MMA rows
 
 @pytest.mark.parametrize("B,Hq,Hkv,Lmax,lens", [
     (3, 16, 1, 700, [700, 129, 1]),          # G = 16; one key; one past a block edge
@@ -217,3 +216,49 @@ def test_wide_group_many_short_sequences_and_repeat(gqa_lib, oracle_mod, cuda_de
     assert torch.equal(a, b)
     assert gqa_lib.gqa_get_device_status() == 0
     assert_parity(a.double().cpu().numpy(), oracle_decode(oracle_mod, q, k, v, sl, w.scale), "wide short")
+
+
+# ---- wide groups over many (b, kv head) pairs: equal shares of the flattened
+# block space cut pairs into two to many pieces (merged by the CTA that
+# completes each pair's count), including pairs longer than several shares.
+
+def _many_pairs_case(B, Hq, Hkv, Lmax, lens, seed, q_mult=1.0):
+    w = W.DecodeWorkload("many_pairs", B, Hq, Hkv, 128, Lmax, 1, Lmax, seed)
+    q, k, v, _ = W.make_decode_inputs(w, q_mult=q_mult)
+    return w, q, k, v, torch.tensor(lens, dtype=torch.int32)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,lens", [
+    (16, 32, 1, 5120, [5120, 1024] * 8),   # 40-block pairs among 8-block pairs
+    # G = 16, four KV heads: 64 pairs of ragged length
+    (16, 64, 4, 1024, [1024, 1, 700, 129, 512, 900, 33, 256, 640, 1000, 77, 128, 384, 1023, 255, 800]),
+    (32, 18, 2, 600, [600 - 17 * i for i in range(32)]),  # G = 9, two KV heads
+    (16, 16, 1, 9472, [9472] + [100] * 15),  # one 74-block pair among 15 one-block pairs
+    (16, 32, 1, 8192, [8192] * 16),          # equal 64-block pairs
+])
+def test_wide_group_many_pairs(gqa_lib, oracle_mod, cuda_device, B, Hq, Hkv, Lmax, lens):
+    w, q, k, v, sl = _many_pairs_case(B, Hq, Hkv, Lmax, lens, 4000 + B * Hq + Lmax)
+    out, flags = run_decode(gqa_lib, q, k, v, sl, w.scale, cuda_device)
+    assert flags == 0
+    assert_parity(out, oracle_decode(oracle_mod, q, k, v, sl, w.scale), f"many pairs {B},{Hq},{Hkv},{Lmax}")
+
+
+def test_wide_group_many_pairs_edges_and_repeat(gqa_lib, oracle_mod, cuda_device):
+    """Many pairs with NaN past every sequence end, q x 8, an empty context
+    and a clamped length; two calls give identical bits."""
+    lens = [1500, 1, 700, 0, 5000, 333, 1024, 1499, 128, 129, 1, 64, 900, 1200, 10, 1500, 777, 256, 1400, 3]
+    w, q, k, v, sl = _many_pairs_case(20, 32, 1, 1500, lens, 4321, q_mult=8.0)
+    W.poison_tail(k, v, sl.clamp(max=1500))
+    d = cuda_device
+    qd, kd, vd, sld = q.to(d), k.to(d), v.to(d), sl.to(d)
+    a = gqa_lib.gqa_decode(qd, kd, vd, sld, scale=w.scale).clone()
+    assert gqa_lib.gqa_get_device_status() == (gqa_lib.GQA_DEV_EMPTY_CONTEXT | gqa_lib.GQA_DEV_SEQLEN_CLAMPED)
+    b = gqa_lib.gqa_decode(qd, kd, vd, sld, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert gqa_lib.gqa_get_device_status() == (gqa_lib.GQA_DEV_EMPTY_CONTEXT | gqa_lib.GQA_DEV_SEQLEN_CLAMPED)
+    out = a.double().cpu().numpy()
+    assert np.all(out[3] == 0)
+    ref = oracle_decode(oracle_mod, q, k, v, sl.clamp(min=1, max=1500), w.scale)
+    keep = [i for i in range(20) if i != 3]
+    assert_parity(out[keep], ref[keep], "many pairs edges")
