@@ -135,8 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pub_full = e8_empty + S8b;  // [2] partial slot 0 / 1 written (bf16 cache: merged by warps 2-3)
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
   volatile int* abort_flag = misc;
-  volatile int* merge_flag = misc + 1;
-  volatile int* chi_flag = misc + 2;
+  volatile int* merge_flags = misc + 4;  // [2][2]: last-piece flag and owner of the last piece, per publisher
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 3);
   int* scan = misc + 8;  // [8]
 
@@ -255,8 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // slot: count it in; the CTA whose piece completes the pair's count merges
   // all the pieces into the output.  Run by the nthr threads r = 0 .. nthr-1
   // that meet at named barrier bar_id (every one of them, also after an
-  // abort, so that the barrier counts always match).
-  auto publish_merge = [&](const Iter& it, __nv_bfloat16* outp, int r, int nthr, int bar_id) {
+  // abort, so that the barrier counts always match); flag 0 or 1 picks the
+  // shared words it broadcasts through (the softmax group and warps 2-3 may
+  // publish at the same time).
+  auto publish_merge = [&](const Iter& it, __nv_bfloat16* outp, int r, int nthr, int bar_id, int flag) {
+    volatile int* merge_flag = merge_flags + 2 * flag;
+    volatile int* chi_flag = merge_flag + 1;
     named_bar_sync(bar_id, nthr);
     if (r == 0 && !*abort_flag) {
       const int o_p = Hkv * pre[it.b] + it.j * it.nb;
@@ -572,10 +575,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = s_c; t < e_c; ++t) {
       if (t == s_c || it.lt == 0) seg_lt0 = it.lt;
       const bool last = (t == e_c - 1) || it.lt == it.nb - 1;
-      if (last && !(seg_lt0 == 0 && it.lt == it.nb - 1)) {
+      // cut pieces before the share's last one (that one the softmax group
+      // publishes itself)
+      if (last && t != e_c - 1 && !(seg_lt0 == 0 && it.lt == it.nb - 1)) {
         mbar_wait_bounded(&pub_full[seg_lt0 == 0 ? 1 : 0], 0, abort_flag, p.err, p.wait_ns);
         __nv_bfloat16* outp = p.out + ((size_t)it.b * p.Hq + (size_t)it.j * G) * kD;
-        publish_merge(it, outp, ct, 64, 2);
+        publish_merge(it, outp, ct, 64, 2, 1);
       }
       it_next(it, pre, B, Hkv);
     }
@@ -754,8 +759,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_before_sync();
         if (!complete) {
-          if (KV8) {
-            publish_merge(it, outp, r, 128, 1);
+          if (KV8 || t == e_c - 1) {
+            // the share's last piece (nothing left to overlap with): this
+            // group of 128 threads counts it in and merges, one head per
+            // four threads
+            publish_merge(it, outp, r, 128, 1, 0);
           } else {
             // warps 2-3 count the piece in and merge; this group goes on
             mbar_arrive(&pub_full[slot]);
