@@ -52,18 +52,18 @@ HEADLINE = "llama3_8b"
 # null as soon as the source differs.
 NCU_TRAFFIC = {
     ("decode.cu", "llama3_8b"): {
-        "sha256": "dee2bfbdfe9ded3fbc0521e5e9feb3b9dc94273b8aced84892372ae489d22684",
-        "bytes_per_launch": 268628224.0 + 2698496.0,
+        "sha256": "26f13e18600d1df4cb7d0b703718bfd2a90ff1fc3fa93aac664eeb88345b1077",
+        "bytes_per_launch": 268648448.0 + 2705152.0,
         "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum, one launch of "
                    "python bench.py --only llama3_8b --steps 3 --warmup 3"},
     ("decode_tc.cu", "mqa"): {
-        "sha256": "c554577702287cb585c9054784a31825f8949a60f8c7c12d1f261c5ea8f5b2f2",
-        "bytes_per_launch": 44314624.0 + 39680.0,
+        "sha256": "346960d92c236ce782c0091ee4e6b538001270e9599d8af30c58832d5e70ba00",
+        "bytes_per_launch": 44320256.0 + 36096.0,
         "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum, one launch of "
                    "python bench.py --only mqa --steps 3 --warmup 3"},
     ("prefill.cu", "prefill"): {
-        "sha256": "1e59f1301d937b20adbf4169bd50c44a4fc7a38527a3436746f6582366487f44",
-        "bytes_per_launch": 100820992.0 + 14540288.0,
+        "sha256": "49ae9b16a18d68d9188749b389271f3474d5de3d207fe4995edf217030fd0403",
+        "bytes_per_launch": 100837376.0 + 14577920.0,
         "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum, one launch of "
                    "python bench.py --only prefill --steps 3 --warmup 3"},
 }
