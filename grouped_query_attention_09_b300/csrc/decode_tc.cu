@@ -1,5 +1,6 @@
 // decode_tc.cu -- split-KV GQA decode on the tcgen05 tensor cores, for wide
-// groups (16 <= G <= 128 query heads per KV head, e.g. multi-query attention).
+// groups (9 <= G <= 128 query heads per KV head at D = 128, e.g. multi-query
+// attention).
 //
 // Same computation as decode.cu: for every sequence b and query head h, the
 // new query attends to the first seqlens[b] rows of KV head j = h / G of the
@@ -25,12 +26,16 @@
 //           elected lane issues): S_i = Q K_i^T into S buffer i % 2, then
 //           O += P_{i-1} V_{i-1} -- the next block's scores are computed while
 //           the softmax of the current one runs.
+//   warps 2-3  bf16 cache: publisher of the cut pieces before the share's
+//           last one (count the piece in; the CTA that completes a pair's
+//           count merges it).  FP8 cache: E4M3 -> fp16 converters (below).
 //   warps 4-7  softmax and epilogue, one thread per query head (TMEM lane):
 //           mask keys past seqlens[b], running max (re-based only when it
 //           grows by more than 2^8), P = exp2(.) as bf16 over the S buffer,
 //           running sum; at the end of a piece, O / l to the output or the
-//           partial slot.  Warps whose 32 lanes are all padding rows skip the
-//           TMEM work but keep the barrier protocol.
+//           partial slot (publishing the share's last cut piece itself).
+//           Warps whose 32 lanes are all padding rows skip the TMEM work but
+//           keep the barrier protocol.
 // TMEM: S buffers at columns [0, 128) and [128, 256), O at [256, 384).
 //
 // Every wait is bounded; on expiry GQA_DEV_WAIT_TIMEOUT is flagged, the roles

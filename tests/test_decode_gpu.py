@@ -169,13 +169,13 @@ def test_side_stream_and_host_entry_point(gqa_lib, cuda_device):
 @pytest.mark.parametrize("B,Hq,Hkv,Lmax,lens", [
     (3, 16, 1, 700, [700, 129, 1]),          # G = 16; one key; one past a block edge
     (2, 24, 1, 400, [400, 255]),             # G = 24 (not a power of two)
-    (3, 36, 3, 260, [260, 1, 200]),          # G = 12 (between the two kernels' ranges)
+    (3, 36, 3, 260, [260, 1, 200]),          # G = 12
     (2, 64, 1, 1000, [1000, 513]),           # G = 64: two warps of heads
     (1, 128, 1, 384, [384]),                 # G = 128: every TMEM lane a head
     (4, 64, 2, 900, [900, 128, 127, 640]),   # G = 32, two KV heads; block-exact lengths
-    (2, 9, 1, 500, [500, 77]),               # G = 9: smallest group on the keys-in-M kernel
-    (2, 34, 2, 300, [300, 129]),             # G = 17: first group padded to 32 columns
-    (1, 33, 1, 256, [256]),                  # G = 33: smallest group with heads as the MMA rows
+    (2, 9, 1, 500, [500, 77]),               # G = 9: smallest group on the tcgen05 kernel
+    (2, 34, 2, 300, [300, 129]),             # G = 17
+    (1, 33, 1, 256, [256]),                  # G = 33: rows of a second lane quarter
     (5, 80, 4, 1500, [1500, 1, 384, 1023, 700]),  # G = 20, four KV heads (whole-pair shares)
     (2, 32, 1, 8192, [8192, 300]),          # one long pair cut into many pieces (split shares, > 4 pieces)
     (4, 64, 2, 4096, [4096, 100, 2000, 4096]),  # G = 32, split shares over every SM, cut pairs
