@@ -57,8 +57,8 @@ NCU_TRAFFIC = {
         "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum, one launch of "
                    "python bench.py --only llama3_8b --steps 3 --warmup 3"},
     ("decode_tc.cu", "mqa"): {
-        "sha256": "346960d92c236ce782c0091ee4e6b538001270e9599d8af30c58832d5e70ba00",
-        "bytes_per_launch": 44320256.0 + 36096.0,
+        "sha256": "c3617e4f2943e1d0b60f08751aae264e757ae05e7901a99ac6fd64955347ff72",
+        "bytes_per_launch": 44320512.0 + 34048.0,
         "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum, one launch of "
                    "python bench.py --only mqa --steps 3 --warmup 3"},
     ("prefill.cu", "prefill"): {
