@@ -158,3 +158,15 @@ def test_fp8_rejects_d64_wide_groups(gqa_lib, cuda_device):
     with pytest.raises(gqa_lib.GQAError) as e:
         gqa_lib.gqa_decode_fp8(q, k8, k8, sc, sc, sl, scale=w.scale)
     assert e.value.status == gqa_lib.GQA_ERR_UNSUPPORTED
+
+
+def test_fp8_max_batch(gqa_lib, oracle_mod, cuda_device):
+    """B = 1024 short ragged sequences with an E4M3 cache (G = 4 and G = 32)."""
+    for Hq, Hkv, Lmax in ((8, 2, 64), (32, 1, 256)):
+        g = torch.Generator().manual_seed(91 + Hq)
+        sl = torch.randint(1, Lmax + 1, (1024,), generator=g, dtype=torch.int32)
+        w = W.DecodeWorkload("fp8_maxb", 1024, Hq, Hkv, 128, Lmax, 1, Lmax, 700 + Hq)
+        q, k8, v8, ks, vs, _ = W.make_decode_fp8_inputs(w)
+        out, flags = run_fp8(gqa_lib, q, k8, v8, ks, vs, sl, w.scale, cuda_device)
+        assert flags == 0
+        assert_parity(out, oracle_fp8(oracle_mod, q, k8, v8, ks, vs, sl, w.scale), f"fp8 max batch G={Hq // Hkv}")

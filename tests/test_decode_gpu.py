@@ -262,3 +262,35 @@ def test_wide_group_many_pairs_edges_and_repeat(gqa_lib, oracle_mod, cuda_device
     ref = oracle_decode(oracle_mod, q, k, v, sl.clamp(min=1, max=1500), w.scale)
     keep = [i for i in range(20) if i != 3]
     assert_parity(out[keep], ref[keep], "many pairs edges")
+
+
+# ---- limits: the largest batch the kernels take (B = 1024: the per-CTA
+# prefix scan of the lengths holds 1025 entries), and a long context.
+
+@pytest.mark.parametrize("Hq,Hkv,Lmax", [(8, 2, 64), (32, 1, 256)])
+def test_max_batch(gqa_lib, oracle_mod, cuda_device, Hq, Hkv, Lmax):
+    """B = 1024 short ragged sequences, some empty: both kernels (G = 4 on the
+    warp-level kernel, G = 32 on the tcgen05 kernel)."""
+    g = torch.Generator().manual_seed(77 + Hq)
+    sl = torch.randint(0, Lmax + 1, (1024,), generator=g, dtype=torch.int32)
+    w = W.DecodeWorkload("maxb", 1024, Hq, Hkv, 128, Lmax, 1, Lmax, 500 + Hq)
+    q, k, v, _ = W.make_decode_inputs(w)
+    out, flags = run_decode(gqa_lib, q, k, v, sl, w.scale, cuda_device)
+    empty = sl <= 0
+    assert flags == (gqa_lib.GQA_DEV_EMPTY_CONTEXT if bool(empty.any()) else 0)
+    assert np.all(out[empty.numpy()] == 0)
+    keep = (~empty).numpy()
+    ref = oracle_decode(oracle_mod, q, k, v, sl.clamp(min=1), w.scale)
+    assert_parity(out[keep], ref[keep], f"max batch G={Hq // Hkv}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (16, 1)])
+def test_long_context(gqa_lib, oracle_mod, cuda_device, Hq, Hkv):
+    """131072 cached keys (1024 or 2048 tiles in one pair): the pair is cut
+    into many pieces on both kernels."""
+    w = W.DecodeWorkload("long", 2, Hq, Hkv, 128, 131072, 1, 131072, 600 + Hq)
+    q, k, v, _ = W.make_decode_inputs(w)
+    sl = torch.tensor([131072, 70001], dtype=torch.int32)
+    out, flags = run_decode(gqa_lib, q, k, v, sl, w.scale, cuda_device)
+    assert flags == 0
+    assert_parity(out, oracle_decode(oracle_mod, q, k, v, sl, w.scale), f"long context G={Hq // Hkv}")
