@@ -82,16 +82,33 @@ int get_ctx(DeviceCtx** out) {
   return GQA_OK;
 }
 
-// Orders this call after the previous workspace user if it ran on another stream.
+// True while `s` is being captured into a CUDA graph: nothing may then
+// synchronise, allocate, or wait on an event recorded outside the capture.
+bool capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  return cudaStreamIsCapturing(s, &st) == cudaSuccess && st != cudaStreamCaptureStatusNone;
+}
+
+// Orders this call after the previous workspace user if it ran on another
+// stream.  A captured call is not ordered here: replays of a graph are
+// ordered against other users of the workspace by the caller.
 cudaError_t order_after_previous(DeviceCtx& c, cudaStream_t s) {
+  if (capturing(s)) return cudaSuccess;
   if (c.evt_pending && c.last_stream != s) return cudaStreamWaitEvent(s, c.last_evt, 0);
   return cudaSuccess;
 }
 
 cudaError_t mark_used(DeviceCtx& c, cudaStream_t s) {
+  if (capturing(s)) return cudaSuccess;
   c.last_stream = s;
   c.evt_pending = true;
   return cudaEventRecord(c.last_evt, s);
+}
+
+int capture_needs_growth() {
+  g_cuda_msg = "the workspace must grow, which cannot happen during stream capture: make one call with these "
+               "sizes (or larger) before capturing";
+  return GQA_ERR_CUDA;
 }
 
 int check_decode_args(const void* q, const void* k, const void* v, const int32_t* seqlens,
@@ -130,6 +147,7 @@ int decode_locked(DeviceCtx& c, const void* q, const void* k, const void* v, con
   if (!gqa::decode_plan(B, Hq, Hkv, D, Lmax, c.sm_count, &plan, 0, kv8)) return GQA_ERR_UNSUPPORTED;
   cudaError_t e;
   if (plan.ws_part_floats > c.ws_part_cap || plan.ws_counters > c.counters_cap) {
+    if (capturing(s)) return capture_needs_growth();
     // Growing the workspace: cudaFree waits for work that still uses the old one.
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
     if (plan.ws_part_floats > c.ws_part_cap) {
@@ -160,6 +178,7 @@ int decode_locked(DeviceCtx& c, const void* q, const void* k, const void* v, con
 
 cudaError_t ensure_stage(DeviceCtx& c, size_t bytes, cudaStream_t s) {
   if (bytes <= c.stage_cap) return cudaSuccess;
+  if (capturing(s)) return cudaErrorStreamCaptureUnsupported;
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return e;
   if (c.stage) cudaFree(c.stage);
@@ -443,7 +462,7 @@ const char* gqa_status_string(int status) {
   switch (status) {
     case GQA_OK: return "GQA_OK";
     case GQA_ERR_INVALID_ARG: return "GQA_ERR_INVALID_ARG: a size is <= 0, Hq % Hkv != 0, causal is not 0/1 or scale is not finite and > 0";
-    case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED: shape not implemented (decode: D = 128 with Hq/Hkv <= 128, or D = 64 with Hq/Hkv <= 8, 16 or 32; B <= 1024; prefill: D == 128)";
+    case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED: shape not implemented (decode: D = 128 with Hq/Hkv <= 128, or D = 64 with Hq/Hkv <= 8, 16 or 32; B <= 1024; prefill: D = 64 or 128)";
     case GQA_ERR_NULL: return "GQA_ERR_NULL: a required pointer is NULL";
     case GQA_ERR_MISALIGNED: return "GQA_ERR_MISALIGNED: tensor pointers must be 16-byte aligned (seqlens 4-byte)";
     case GQA_ERR_CUDA: {

@@ -31,6 +31,17 @@
  *     serialises access to its per-device workspace.  Two decode calls that
  *     share the workspace must not run concurrently on different streams; the
  *     library orders them on the stream of the later call.
+ *   - CUDA graphs: the device entry points can be captured (stream capture)
+ *     once a call with the same or larger sizes has run outside the capture,
+ *     so that nothing has to be allocated; a call that would have to grow the
+ *     workspace during capture returns GQA_ERR_CUDA and enqueues nothing.
+ *     Captured calls are not ordered against other users of the workspace by
+ *     the library: the caller orders a graph's replays against decode calls
+ *     on other streams (replays on the capturing stream's successors, or on
+ *     the stream the direct calls use, need nothing).  Every replay reads the
+ *     inputs' current contents (new q, cache rows and seqlens values in the
+ *     same buffers) and the in-launch merge counters return to zero at the
+ *     end of each launch, so a graph replays any number of times.
  */
 #ifndef GQA_H_
 #define GQA_H_
