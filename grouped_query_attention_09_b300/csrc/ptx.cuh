@@ -231,17 +231,6 @@ __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, f
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
-// (d0, d1) += (a0, a1) as one packed f32x2 add.
-__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
-  asm("{\n\t.reg .b64 ra, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rd, {%0, %1};\n\t"
-      "add.f32x2 rd, rd, ra;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "+f"(d0), "+f"(d1)
-      : "f"(a0), "f"(a1));
-}
-
 // Named barrier over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
