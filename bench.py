@@ -449,6 +449,12 @@ def run_only(g, W, args, dev, flush, peaks):
         tf = r["flops"] / (ms / 1e3) / 1e12
         print(json.dumps({"only": args.only, "us": ms * 1e3, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]}))
         return 0
+    if args.only == "prefill_chunk":
+        r = bench_prefill_chunk(g, W, dev, args.steps, args.warmup, flush)
+        ms = statistics.mean(r["ms"])
+        tf = r["flops"] / (ms / 1e3) / 1e12
+        print(json.dumps({"only": args.only, "us": ms * 1e3, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]}))
+        return 0
     if args.only.endswith("_paged"):
         name = args.only[:-6]
         r = bench_decode_paged(g, W, name, 128 if name == "mqa" else 256, dev, args.steps, args.warmup, flush)
@@ -489,7 +495,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="headline only (for profiling runs)")
     ap.add_argument("--only", default=None,
                     help="time one workload and print its line: a decode workload name (tiny, llama3_8b, "
-                         "llama2_70b, mqa), optionally with _fp8 or _paged; prefill; prefill_d64; rope_append; kv_meanpool")
+                         "llama2_70b, mqa), optionally with _fp8 or _paged; prefill; prefill_d64; prefill_chunk; rope_append; "
+                         "kv_meanpool")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
