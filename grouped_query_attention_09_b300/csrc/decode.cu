@@ -241,16 +241,32 @@ __global__ void __launch_bounds__(288, 1)
     // when the lengths are equal this CTA's share is exactly pair blockIdx.x,
     // so its first tiles are pulled into L2 while the prologue below reads
     // seqlens (with unequal lengths the prefetch is merely wasted).  The rows
-    // stay inside the tensor map: at most Lmax.
+    // stay inside the tensor map: at most Lmax.  A paged cache maps each
+    // tile through the block table first (row t kBN of pair (b, j) sits in
+    // page block_table[b][t kBN / page_size]); an entry outside the page pool
+    // is skipped here (the producer flags it when it loads the tile).
+    const int pb = (int)blockIdx.x / Hkv, pj = (int)blockIdx.x - pb * Hkv;
+    int pg_lp = -1, pg = -1;
     for (int t = 0; t < p.prefetch_tiles; ++t) {
+      int y = t * kBN, z = (int)blockIdx.x;
+      if (p.block_table) {
+        const int lp = y / p.page_size;
+        if (lp != pg_lp) {
+          pg_lp = lp;
+          pg = __ldg(p.block_table + (size_t)pb * p.max_pages + lp);
+        }
+        if (pg < 0 || pg >= p.num_pages) continue;
+        z = pg * Hkv + pj;
+        y -= lp * p.page_size;
+      }
       if constexpr (KV8) {
-        tma_prefetch_l2_3d(&tmK, 0, t * kBN, blockIdx.x);
-        tma_prefetch_l2_3d(&tmV, 0, t * kBN, blockIdx.x);
+        tma_prefetch_l2_3d(&tmK, 0, y, z);
+        tma_prefetch_l2_3d(&tmV, 0, y, z);
       } else {
 #pragma unroll
         for (int box = 0; box < D / 64; ++box) {
-          tma_prefetch_l2_3d(&tmK, box * 64, t * kBN, blockIdx.x);
-          tma_prefetch_l2_3d(&tmV, box * 64, t * kBN, blockIdx.x);
+          tma_prefetch_l2_3d(&tmK, box * 64, y, z);
+          tma_prefetch_l2_3d(&tmV, box * 64, y, z);
         }
       }
     }
@@ -981,8 +997,7 @@ cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t s
   p.wait_ns = pipeline_wait_limit_ns();
   p.starve = pipeline_starved() ? 1 : 0;
   p.prefetch_tiles = 0;
-  if (!a.block_table && plan.num_ctas == a.B * a.Hkv)
-    p.prefetch_tiles = std::min(plan.stages, (a.Lmax + kBN - 1) / kBN);
+  if (plan.num_ctas == a.B * a.Hkv) p.prefetch_tiles = std::min(plan.stages, (a.Lmax + kBN - 1) / kBN);
   if (a.block_table && (a.page_size % kBN != 0 || a.page_size <= 0)) return cudaErrorInvalidValue;
   auto kern = decode_kernel<D, NT, KV8>;
   // The opt-in shared-memory size is a per-device function attribute: set it
