@@ -21,7 +21,7 @@ Under torchrun (N > 1) every rank runs its own batch of the same shape
 the bytes of all ranks divided by the slowest rank's time.
 
 Also timed in the same run (reported as extra keys): FP8 (E4M3) cache decode,
-paged-cache decode, the rotary embedding + cache append of the new token, a
+paged-cache decode (bf16 and FP8 pages), the rotary embedding + cache append of the new token, a
 chunked prefill after a cached prefix, and the MHA -> GQA mean-pool conversion
 of a K projection.
 
@@ -52,13 +52,13 @@ HEADLINE = "llama3_8b"
 # null as soon as the source differs.
 NCU_TRAFFIC = {
     ("decode.cu", "llama3_8b"): {
-        "sha256": "441a256c89914401999732030f75bfe6c52908b8fa2dde1e05073716496aec06",
-        "bytes_per_launch": 268637952.0 + 3084032.0,
+        "sha256": "805168c27d502c7b9a2b9c7bd946e399a660a4f412a063d7c2d95e5cbfe8246b",
+        "bytes_per_launch": 268639232.0 + 2390016.0,
         "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum, one launch of "
                    "python bench.py --only llama3_8b --steps 3 --warmup 3"},
     ("decode_tc.cu", "mqa"): {
-        "sha256": "c3617e4f2943e1d0b60f08751aae264e757ae05e7901a99ac6fd64955347ff72",
-        "bytes_per_launch": 44320512.0 + 34048.0,
+        "sha256": "2fe2a8f7fbb80615831d71f094ab0487200f592a3f237431e344a05edbf23241",
+        "bytes_per_launch": 44320256.0 + 33280.0,
         "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum, one launch of "
                    "python bench.py --only mqa --steps 3 --warmup 3"},
     ("prefill.cu", "prefill"): {
@@ -238,6 +238,26 @@ def bench_decode_paged(g, W, name, page_size, dev, steps, warmup, flush):
     if flags:
         raise RuntimeError(f"decode paged {name}: device status {flags:#x}")
     return {"w": w, "ms": ts, "bytes": W.decode_kv_bytes(sl, w.Hkv, w.D)}
+
+
+def bench_decode_fp8_paged(g, W, name, page_size, dev, steps, warmup, flush):
+    """gqa_decode_fp8_paged on workload `name`: its E4M3 cache cut into pages
+    of page_size rows, handed out in a seeded random order."""
+    import torch
+    w = W.WORKLOADS[name]
+    q, k8, v8, ks, vs, sl = W.make_decode_fp8_inputs(w)
+    kp, vp, bt = W.page_cache(k8, v8, page_size, seed=w.seed + 60)
+    del k8, v8
+    qd, kd, vd, ksd, vsd, btd, sld = (t.to(dev) for t in (q, kp, vp, ks, vs, bt, sl))
+    out = torch.empty_like(qd)
+    stream = torch.cuda.current_stream(dev)
+    ts = timed_launches(lambda: g.gqa_decode_fp8_paged(qd, kd, vd, ksd, vsd, btd, sld, out=out, scale=w.scale,
+                                                       stream=stream),
+                        steps, warmup, flush, stream)
+    flags = g.gqa_get_device_status()
+    if flags:
+        raise RuntimeError(f"decode fp8 paged {name}: device status {flags:#x}")
+    return {"w": w, "ms": ts, "bytes": W.decode_kv_bytes_fp8(sl, w.Hkv, w.D)}
 
 
 def bench_rope_append(g, W, name, dev, steps, warmup, flush):
@@ -455,6 +475,13 @@ def run_only(g, W, args, dev, flush, peaks):
         tf = r["flops"] / (ms / 1e3) / 1e12
         print(json.dumps({"only": args.only, "us": ms * 1e3, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]}))
         return 0
+    if args.only.endswith("_fp8_paged"):
+        name = args.only[:-10]
+        r = bench_decode_fp8_paged(g, W, name, 128 if name == "mqa" else 256, dev, args.steps, args.warmup, flush)
+        ms = statistics.mean(r["ms"])
+        gbs = r["bytes"] / (ms / 1e3) / 1e9
+        print(json.dumps({"only": args.only, "us": ms * 1e3, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}))
+        return 0
     if args.only.endswith("_paged"):
         name = args.only[:-6]
         r = bench_decode_paged(g, W, name, 128 if name == "mqa" else 256, dev, args.steps, args.warmup, flush)
@@ -495,7 +522,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="headline only (for profiling runs)")
     ap.add_argument("--only", default=None,
                     help="time one workload and print its line: a decode workload name (tiny, llama3_8b, "
-                         "llama2_70b, mqa), optionally with _fp8 or _paged; prefill; prefill_d64; prefill_chunk; rope_append; "
+                         "llama2_70b, mqa), optionally with _fp8, _paged or _fp8_paged; prefill; prefill_d64; prefill_chunk; rope_append; "
                          "kv_meanpool")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -562,6 +589,14 @@ def main():
             dp[name] = {"page_size": ps, "us": ms * 1e3, "kv_bytes": r["bytes"], "GB/s": gbs,
                         "frac_hbm": gbs / peaks["hbm_gbs"]}
         extras["decode_paged"] = dp
+        d8p = {}
+        for name, ps in (("llama3_8b", 256), ("mqa", 128)):
+            r = bench_decode_fp8_paged(g, W, name, ps, dev, small_steps, args.warmup, flush)
+            ms = statistics.mean(r["ms"])
+            gbs = r["bytes"] / (ms / 1e3) / 1e9
+            d8p[name] = {"page_size": ps, "us": ms * 1e3, "kv_bytes_fp8": r["bytes"], "GB/s": gbs,
+                         "frac_hbm": gbs / peaks["hbm_gbs"]}
+        extras["decode_fp8_paged"] = d8p
         ra = bench_rope_append(g, W, "llama3_8b", dev, small_steps, args.warmup, flush)
         rms = statistics.mean(ra["ms"])
         extras["rope_append"] = {"workload": "new token of llama3_8b: B=16, Hq=32, Hkv=8, D=128, appended at 4095",

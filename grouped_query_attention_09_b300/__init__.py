@@ -6,7 +6,8 @@ status.  All arithmetic runs in the library's CUDA kernels; there is no CPU
 or PyTorch fallback, and a missing or unloadable library raises.
 
 Names and semantics follow include/gqa.h:
-  gqa_decode, gqa_decode_fp8, gqa_decode_paged, gqa_rope_append, gqa_prefill, gqa_prefill_chunk, gqa_decode_host, gqa_prefill_host,
+  gqa_decode, gqa_decode_fp8, gqa_decode_paged, gqa_decode_fp8_paged, gqa_decode_noalloc, gqa_rope_append,
+  gqa_meanpool_kv_heads, gqa_prefill, gqa_prefill_chunk, gqa_decode_host, gqa_prefill_host,
   gqa_status_string, gqa_get_device_status, gqa_decode_plan, gqa_release,
   and the failure-injection hooks gqa_test_set_wait_limit_ns,
   gqa_test_fail_workspace_allocs.
@@ -36,7 +37,8 @@ GQA_DEV_BAD_PAGE = 0x10
 
 EXPORTED = ("gqa_decode", "gqa_prefill", "gqa_decode_host", "gqa_prefill_host",
             "gqa_status_string", "gqa_get_device_status", "gqa_decode_plan", "gqa_release",
-            "gqa_decode_noalloc", "gqa_decode_fp8", "gqa_rope_append", "gqa_decode_paged", "gqa_prefill_chunk",
+            "gqa_decode_noalloc", "gqa_decode_fp8", "gqa_rope_append", "gqa_decode_paged", "gqa_decode_fp8_paged",
+            "gqa_prefill_chunk",
             "gqa_meanpool_kv_heads", "gqa_test_set_wait_limit_ns", "gqa_test_fail_workspace_allocs")
 
 _lib = None
@@ -67,6 +69,8 @@ def load_library():
     lib.gqa_rope_append.restype = i
     lib.gqa_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     lib.gqa_decode_paged.restype = i
+    lib.gqa_decode_fp8_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.gqa_decode_fp8_paged.restype = i
     lib.gqa_prefill_chunk.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.gqa_prefill_chunk.restype = i
     lib.gqa_meanpool_kv_heads.argtypes = [vp, vp, i, i, i, i, i, vp]
@@ -198,6 +202,34 @@ def gqa_decode_paged(q, k_pages, v_pages, block_table, seqlens, out=None, scale=
                                   B, Hq, Hkv, D, num_pages, page_size, max_pages, float(scale),
                                   _stream_ptr(stream, q.device))
     _check(st, "gqa_decode_paged")
+    return out
+
+
+def gqa_decode_fp8_paged(q, k_pages, v_pages, k_scale, v_scale, block_table, seqlens, out=None, scale=None,
+                         stream=None):
+    """Decode over a paged FP8 E4M3 cache.  q [B, Hq, D] bf16; k_pages/v_pages
+    [num_pages, Hkv, page_size, D] uint8; k_scale/v_scale [B, Hkv] fp32;
+    block_table [B, max_pages] int32; seqlens [B] int32 (all device); returns
+    out [B, Hq, D] bf16."""
+    import torch
+    B, Hq, D = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    max_pages = block_table.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = D ** -0.5
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.gqa_decode_fp8_paged(_dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k_pages, "k_pages", torch.uint8),
+                                      _dev_ptr(v_pages, "v_pages", torch.uint8),
+                                      _dev_ptr(k_scale, "k_scale", torch.float32),
+                                      _dev_ptr(v_scale, "v_scale", torch.float32),
+                                      _dev_ptr(block_table, "block_table", torch.int32),
+                                      _dev_ptr(seqlens, "seqlens", torch.int32), _dev_ptr(out, "out", torch.bfloat16),
+                                      B, Hq, Hkv, D, num_pages, page_size, max_pages, float(scale),
+                                      _stream_ptr(stream, q.device))
+    _check(st, "gqa_decode_fp8_paged")
     return out
 
 

@@ -318,6 +318,37 @@ int gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages, co
                        static_cast<cudaStream_t>(stream), nullptr, nullptr, pc);
 }
 
+int gqa_decode_fp8_paged(const void* q, const void* k_pages, const void* v_pages, const float* k_scale,
+                         const float* v_scale, const int32_t* block_table, const int32_t* seqlens, void* out, int B,
+                         int Hq, int Hkv, int D, int num_pages, int page_size, int max_pages, float scale,
+                         void* stream) {
+  if (!q || !k_pages || !v_pages || !k_scale || !v_scale || !block_table || !seqlens || !out) return GQA_ERR_NULL;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_pages <= 0 || page_size <= 0 || max_pages <= 0 ||
+      Hq % Hkv != 0)
+    return GQA_ERR_INVALID_ARG;
+  if ((long long)max_pages * page_size > 0x7fffffffLL) return GQA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(seqlens) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return GQA_ERR_MISALIGNED;
+  const int Lcap = max_pages * page_size;
+  gqa::DecodePlan plan;
+  if (!gqa::decode_plan(B, Hq, Hkv, D, Lcap, 148, &plan, 0, true)) return GQA_ERR_UNSUPPORTED;
+  if (page_size % plan.tile_keys != 0) return GQA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceCtx* c = nullptr;
+  int st = get_ctx(&c);
+  if (st != GQA_OK) return st;
+  PagedCache pc;
+  pc.block_table = block_table;
+  pc.page_size = page_size;
+  pc.num_pages = num_pages;
+  pc.max_pages = max_pages;
+  return decode_locked(*c, q, k_pages, v_pages, seqlens, out, B, Hq, Hkv, D, Lcap, scale,
+                       static_cast<cudaStream_t>(stream), k_scale, v_scale, pc);
+}
+
 int gqa_rope_append(const void* q, const void* k_new, const void* v_new, void* q_out, void* k_cache,
                     void* v_cache, int32_t* seqlens, int B, int Hq, int Hkv, int D, int Lmax, double base,
                     void* stream) {

@@ -330,6 +330,11 @@ __global__ void __launch_bounds__(288, 1)
       iter_seek(it, s_c, pre, B, Hkv);
       long long issued = 0;
       int pg_b = -1, pg_lp = -1, pg = 0;  // last block-table entry read (paged cache)
+      // the previous tile's page and row offset in it: along a pair they
+      // advance by one tile without a division (with 8-bit tiles this loop
+      // runs close to the consumers' pace, so a division by page_size on
+      // every tile shows in the step time)
+      int pv_b = -1, pv_j = -1, pv_lt = -2, pv_lp = 0, pv_off = 0;
       // tile i: group ig = i % NG, use us = (i / NG) % SG of that group's
       // ring, lap = i / (NG SG) (kept incrementally: no divisions per tile)
       int ig = 0, us = 0, lap = 0;
@@ -354,7 +359,23 @@ __global__ void __launch_bounds__(288, 1)
           // Paged cache: logical page y / page_size of sequence b; the entry
           // is reloaded only when the page changes.  A page index out of range
           // is flagged and sent outside the tensor map, where TMA reads zeros.
-          const int lp = y / p.page_size;
+          int lp, off;
+          if (it.b == pv_b && it.j == pv_j && it.lt == pv_lt + 1) {
+            lp = pv_lp;
+            off = pv_off + kBN;
+            if (off == p.page_size) {  // page_size is a multiple of kBN
+              off = 0;
+              ++lp;
+            }
+          } else {
+            lp = y / p.page_size;
+            off = y - lp * p.page_size;
+          }
+          pv_b = it.b;
+          pv_j = it.j;
+          pv_lt = it.lt;
+          pv_lp = lp;
+          pv_off = off;
           if (it.b != pg_b || lp != pg_lp) {
             pg_b = it.b;
             pg_lp = lp;
@@ -365,7 +386,7 @@ __global__ void __launch_bounds__(288, 1)
             }
           }
           z = pg < 0 ? -1 : pg * Hkv + it.j;
-          y -= lp * p.page_size;
+          y = off;
         }
         if constexpr (KV8) {
           // one 128-byte-wide box per tensor: a row of D = 128 E4M3 bytes

@@ -834,7 +834,7 @@ cudaError_t decode_tc_launch(const DecodePlan& plan, const DecodeArgs& a, cudaSt
   const int G = plan.G;
   const bool paged = a.block_table != nullptr;
   if (paged && (a.page_size % kBN != 0 || a.page_size <= 0)) return cudaErrorInvalidValue;
-  if (plan.kv8 && (!a.k_scale || !a.v_scale || paged)) return cudaErrorInvalidValue;
+  if (plan.kv8 && (!a.k_scale || !a.v_scale)) return cudaErrorInvalidValue;
   const uint64_t planes = paged ? (uint64_t)a.num_pages * a.Hkv : pairs;
   const uint64_t rows = paged ? (uint64_t)a.page_size : (uint64_t)a.Lmax;
   // Q viewed as [B * Hkv][G][D]: a 128-row box starting at row 0 reads the

@@ -186,6 +186,26 @@ GQA_API int gqa_decode_paged(const void* q, const void* k_pages, const void* v_p
                              int page_size, int max_pages, float scale, void* stream);
 
 /*
+ * gqa_decode_fp8_paged -- gqa_decode_paged over pages of FP8 E4M3 bytes: the
+ * two cache forms above combined (the usual layout of a serving engine's
+ * quantised cache).  Pages are cut from the sequences' caches, so the scales
+ * stay per (sequence, KV head):
+ *
+ *   k_pages, v_pages  [num_pages, Hkv, page_size, D]  uint8 (E4M3 bytes), device
+ *   k_scale, v_scale  [B, Hkv]  fp32, device (4-byte aligned)
+ *   block_table, seqlens, num_pages, page_size, max_pages as gqa_decode_paged;
+ *   everything else as gqa_decode.
+ *
+ * Arithmetic as gqa_decode_fp8, page rules and GQA_DEV_BAD_PAGE as
+ * gqa_decode_paged; supported shapes as gqa_decode_fp8.  The result is
+ * bit-identical to gqa_decode_fp8 on the contiguous cache the pages hold.
+ */
+GQA_API int gqa_decode_fp8_paged(const void* q, const void* k_pages, const void* v_pages, const float* k_scale,
+                                 const float* v_scale, const int32_t* block_table, const int32_t* seqlens, void* out,
+                                 int B, int Hq, int Hkv, int D, int num_pages, int page_size, int max_pages,
+                                 float scale, void* stream);
+
+/*
  * gqa_rope_append -- the step before a decode: rotary position embedding of
  * the new token and the append of its K/V heads to the cache.  The attention
  * code of the GQA paper notes on 51969.com ("QA 相关") rotates the query and

@@ -170,3 +170,49 @@ def test_fp8_max_batch(gqa_lib, oracle_mod, cuda_device):
         out, flags = run_fp8(gqa_lib, q, k8, v8, ks, vs, sl, w.scale, cuda_device)
         assert flags == 0
         assert_parity(out, oracle_fp8(oracle_mod, q, k8, v8, ks, vs, sl, w.scale), f"fp8 max batch G={Hq // Hkv}")
+
+
+@pytest.mark.parametrize("name,D,page_size", [
+    ("llama3_8b", 128, 256),   # one CTA per pair: the launch-time prefetch walks the block table
+    ("mqa", 128, 128),         # G = 32: the tcgen05 kernel's producer maps 128-key blocks to pages
+    ("ragged_d64", 64, 64),    # D = 64, G = 4, ragged lengths
+])
+def test_fp8_paged_parity_and_bits(gqa_lib, oracle_mod, cuda_device, name, D, page_size):
+    """gqa_decode_fp8_paged over E4M3 pages cut from the workload's cache in a
+    seeded random order: bit-identical to gqa_decode_fp8 on the contiguous
+    cache, and at the oracle's bar."""
+    if name == "ragged_d64":
+        w = W.DecodeWorkload("fp8_paged_d64", 5, 16, 4, D, 900, 1, 900, 3333)
+    else:
+        w = W.WORKLOADS[name]
+    q, k8, v8, ks, vs, sl = W.make_decode_fp8_inputs(w)
+    kp, vp, bt = W.page_cache(k8, v8, page_size, seed=w.seed + 77)
+    d = cuda_device
+    qd, ksd, vsd, sld = q.to(d), ks.to(d), vs.to(d), sl.to(d)
+    out_p = gqa_lib.gqa_decode_fp8_paged(qd, kp.to(d), vp.to(d), ksd, vsd, bt.to(d), sld, scale=w.scale)
+    assert gqa_lib.gqa_get_device_status() == 0
+    out_c = gqa_lib.gqa_decode_fp8(qd, k8.to(d), v8.to(d), ksd, vsd, sld, scale=w.scale)
+    assert gqa_lib.gqa_get_device_status() == 0
+    assert torch.equal(out_p, out_c)
+    assert_parity(out_p.double().cpu().numpy(), oracle_fp8(oracle_mod, q, k8, v8, ks, vs, sl, w.scale),
+                  f"{name} fp8 paged")
+
+
+def test_fp8_paged_bad_entry_is_flagged(gqa_lib, oracle_mod, cuda_device):
+    """A needed block-table entry outside the pool sets GQA_DEV_BAD_PAGE; the
+    other sequences stay exact (both kernels)."""
+    d = cuda_device
+    for Hq, page_size in ((8, 64), (32, 128)):
+        w = W.DecodeWorkload("fp8_paged_bad", 4, Hq, 2, 128, 1000, 1, 1000, 4444 + Hq)
+        q, k8, v8, ks, vs, _ = W.make_decode_fp8_inputs(w)
+        sl = torch.tensor([1000, 37, 512, 800], dtype=torch.int32)
+        kp, vp, bt = W.page_cache(k8, v8, page_size, seed=5)
+        bt[2, 1] = 10 ** 6  # sequence 2 needs its second page
+        out = gqa_lib.gqa_decode_fp8_paged(q.to(d), kp.to(d), vp.to(d), ks.to(d), vs.to(d), bt.to(d), sl.to(d),
+                                           scale=w.scale)
+        assert gqa_lib.gqa_get_device_status() == gqa_lib.GQA_DEV_BAD_PAGE
+        ref = oracle_fp8(oracle_mod, q, k8, v8, ks, vs, sl, w.scale)
+        o = out.double().cpu().numpy()
+        assert np.isfinite(o).all()
+        keep = [0, 1, 3]
+        assert_parity(o[keep], ref[keep], f"fp8 paged G={Hq // 2}, other sequences")
