@@ -21,8 +21,9 @@
 //     the last piece of that pair (an arrival counter) merges the pieces by
 //     log-sum-exp and writes the output -- no second kernel.
 //
-// CTA layout: warps 0..NC-1 consume, warp NC produces.
-//   producer: one lane streams K and V tiles [tile_keys x D] of the cache into
+// CTA layout: warps 0..NC-1 consume, warps NC.. produce (one per tile group).
+//   producers: one lane per tile group streams that group's K and V tiles
+//     [tile_keys x D] of the cache into
 //     a ring of shared-memory stages with 3-D TMA loads (128-byte swizzle,
 //     evict-first L2 policy), an mbarrier pair per stage; with one CTA per
 //     (b, kv head) pair it first prefetches the pair's opening tiles into L2
@@ -79,6 +80,7 @@ struct Params {
   const int32_t* block_table;  // paged cache (else null): [B][max_pages] page of each logical page
   int page_size, max_pages, num_pages;
   int prefetch_tiles;  // > 0: one CTA per (b, kv head) pair; prefetch its first tiles into L2 at launch
+  int NP;              // producer warps: 1, or NG (one per tile group)
   unsigned long long wait_ns;  // pipeline-wait limit
   int starve;                  // test hook: the producer issues no loads
 };
@@ -189,7 +191,7 @@ template <int NT>
 __host__ __device__ constexpr int tile_groups() { return NT == 1 ? 2 : 1; }
 
 template <int D, int NT, bool KV8>
-__global__ void __launch_bounds__(288, 1)
+__global__ void __launch_bounds__(320, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const Params p) {
   constexpr int KT = D / 16;  // 16-wide k-steps over D (QK) and m-tiles over D (PV)
@@ -322,8 +324,16 @@ __global__ void __launch_bounds__(288, 1)
   const long long s_c = active ? T * blockIdx.x / P : 0;
   const long long e_c = active ? T * (blockIdx.x + 1) / P : 0;
 
-  if (warp == NC) {
-    // ============================== producer ==============================
+  if (warp >= NC) {
+    // ============================== producers =============================
+    // With p.NP == NG producer warps, warp NC + g fills the ring of tile
+    // group g: it walks every tile (so that the ring counters and the page
+    // position stay exact) and issues the loads of tiles i with i % NG == g.
+    // With one producer (p.NP == 1) warp NC issues every tile.  Two pay with
+    // 8-bit tiles, which one lane cannot issue fast enough for both groups,
+    // and with whole contiguous pairs; with cut pairs or bf16 pages the
+    // extra warp costs more than it brings (measured).
+    const int pgrp = warp - NC;
     if (lane == 0 && s_c < e_c && !p.starve) {
       const uint64_t pol = l2_policy_evict_first();
       TileIter it;
@@ -341,7 +351,8 @@ __global__ void __launch_bounds__(288, 1)
       for (long long t = s_c; t < e_c; ++t) {
         const int i = (int)(t - s_c);
         const int s = ig * SG + us;
-        if (lap > 0) {
+        const bool mine = p.NP == 1 || ig == pgrp;
+        if (mine && lap > 0) {
           if (!mbar_wait_bounded(&empty[s], (uint32_t)((lap - 1) & 1), abort_flag, p.err, p.wait_ns)) break;
         }
         if (++ig == NG) {
@@ -353,7 +364,6 @@ __global__ void __launch_bounds__(288, 1)
         }
         uint8_t* kdst = smem + s * L.stage_bytes;
         uint8_t* vdst = kdst + L.k_bytes;
-        mbar_arrive_expect_tx(&full[s], L.stage_bytes);
         int z = it.b * Hkv + it.j, y = it.lt * kBN;
         if (p.block_table) {
           // Paged cache: logical page y / page_size of sequence b; the entry
@@ -376,7 +386,7 @@ __global__ void __launch_bounds__(288, 1)
           pv_lt = it.lt;
           pv_lp = lp;
           pv_off = off;
-          if (it.b != pg_b || lp != pg_lp) {
+          if (mine && (it.b != pg_b || lp != pg_lp)) {
             pg_b = it.b;
             pg_lp = lp;
             pg = __ldg(p.block_table + (size_t)it.b * p.max_pages + lp);
@@ -388,6 +398,11 @@ __global__ void __launch_bounds__(288, 1)
           z = pg < 0 ? -1 : pg * Hkv + it.j;
           y = off;
         }
+        if (!mine) {
+          iter_next(it, pre, B, Hkv);
+          continue;
+        }
+        mbar_arrive_expect_tx(&full[s], L.stage_bytes);
         if constexpr (KV8) {
           // one 128-byte-wide box per tensor: a row of D = 128 E4M3 bytes
           tma_load_3d(kdst, &tmK, 0, y, z, &full[s], pol);
@@ -403,9 +418,11 @@ __global__ void __launch_bounds__(288, 1)
         iter_next(it, pre, B, Hkv);
       }
       // Wait (bounded) until every copy this thread issued has landed.
-      // The last NG * SG tiles hold the latest use of every stage.
+      // The last NG * SG tiles hold the latest use of every stage; this
+      // producer waits for those of its own group.
       const long long first = issued > NG * SG ? issued - NG * SG : 0;
       for (long long i = first; i < issued; ++i) {
+        if (p.NP != 1 && (int)(i % NG) != pgrp) continue;
         const unsigned long long t0 = globaltimer_ns();
         while (!mbar_try_wait(&full[stage_of(i)], parity_of(i))) {
           if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -1019,6 +1036,9 @@ cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t s
   p.starve = pipeline_starved() ? 1 : 0;
   p.prefetch_tiles = 0;
   if (plan.num_ctas == a.B * a.Hkv) p.prefetch_tiles = std::min(plan.stages, (a.Lmax + kBN - 1) / kBN);
+  // One producer warp per tile group for an 8-bit cache and for whole
+  // contiguous pairs, else one (the measured better choice in each case).
+  p.NP = (KV8 || (!a.block_table && plan.num_ctas == a.B * a.Hkv)) ? tile_groups<NT>() : 1;
   if (a.block_table && (a.page_size % kBN != 0 || a.page_size <= 0)) return cudaErrorInvalidValue;
   auto kern = decode_kernel<D, NT, KV8>;
   // The opt-in shared-memory size is a per-device function attribute: set it
@@ -1031,7 +1051,7 @@ cudaError_t launch_t(const DecodePlan& plan, const DecodeArgs& a, cudaStream_t s
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set.fetch_or(1ull << dev);
   }
-  kern<<<plan.num_ctas, plan.threads, plan.smem_bytes, stream>>>(tmK, tmV, p);
+  kern<<<plan.num_ctas, 32 * (p.NC + p.NP), plan.smem_bytes, stream>>>(tmK, tmV, p);
   return cudaGetLastError();
 }
 
@@ -1068,7 +1088,7 @@ bool decode_plan(int B, int Hq, int Hkv, int D, int Lmax, int sm_count, DecodePl
   plan->HS = HS;
   plan->tile_keys = kBN;
   const int NG = NT == 1 ? tile_groups<1>() : tile_groups<2>();
-  plan->threads = 32 * (kKW * HS * NG + 1);
+  plan->threads = 32 * (kKW * HS * NG + NG);  // at most: NG groups of 4 x HS consumer warps, a producer warp each
   const long long tiles_max = (long long)B * Hkv * ((Lmax + kBN - 1) / kBN);
   plan->num_ctas = (int)std::min<long long>(tiles_max, std::min(kMaxCtas, std::max(1, sm_count)));
   {
