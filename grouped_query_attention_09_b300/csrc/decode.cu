@@ -21,13 +21,14 @@
 //     the last piece of that pair (an arrival counter) merges the pieces by
 //     log-sum-exp and writes the output -- no second kernel.
 //
-// CTA layout: warps 0..NC-1 consume, warps NC.. produce (one per tile group).
-//   producers: one lane per tile group streams that group's K and V tiles
-//     [tile_keys x D] of the cache into
-//     a ring of shared-memory stages with 3-D TMA loads (128-byte swizzle,
-//     evict-first L2 policy), an mbarrier pair per stage; with one CTA per
-//     (b, kv head) pair it first prefetches the pair's opening tiles into L2
-//     while the prologue reads seqlens;
+// CTA layout: warps 0..NC-1 consume, warps NC.. produce.
+//   producers: one lane of a warp streams K and V tiles [tile_keys x D] of
+//     the cache into a ring of shared-memory stages with 3-D TMA loads
+//     (128-byte swizzle, evict-first L2 policy), an mbarrier pair per stage;
+//     for an 8-bit cache or whole contiguous pairs each tile group has its own
+//     producer warp and ring part, otherwise one producer fills both; with one
+//     CTA per (b, kv head) pair the first producer prefetches the pair's
+//     opening tiles into L2 while the prologue reads seqlens;
 //   consumers: NG tile groups (two for G <= 8) of a 4 x HS grid of warps take
 //     alternate tiles, each group from a private part of the ring and walking
 //     only its own tiles; warp (ks, hs) owns keys [16 ks, 16 ks + 16) of its
