@@ -44,3 +44,19 @@ def test_seeded_inputs_are_reproducible():
     for x, y in zip(a, b):
         assert x.equal(y)
     assert int(a[3].min()) >= 3 and int(a[3].max()) <= 16
+
+
+def test_cpu_baseline_sampler_cycles_whole_steps():
+    """bench.py's CPU baseline: with cycling, a step shorter than the budget is
+    timed repeatedly (the sample names whole steps, the rate is the step's K/V
+    bytes over the mean step time); without it, one step at most."""
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    gbs, step_s, sample, threads = bench.oracle_decode_rate(W, "tiny", budget_s=0.3, cycle=True)
+    w = W.WORKLOADS["tiny"]
+    nbytes = W.decode_kv_bytes(W.make_decode_inputs(w)[3], w.Hkv, w.D)
+    assert "steps of" in sample and threads >= 1 and step_s > 0
+    assert abs(gbs - nbytes / step_s / 1e9) <= 1e-9 * gbs
+    _, _, one, _ = bench.oracle_decode_rate(W, "tiny", budget_s=0.3, cycle=False)
+    assert "of one step" in one
