@@ -216,3 +216,27 @@ def test_fp8_paged_bad_entry_is_flagged(gqa_lib, oracle_mod, cuda_device):
         assert np.isfinite(o).all()
         keep = [0, 1, 3]
         assert_parity(o[keep], ref[keep], f"fp8 paged G={Hq // 2}, other sequences")
+
+
+def test_fp8_paged_nan_tail(gqa_lib, oracle_mod, cuda_device):
+    """E4M3 NaN bytes in every row past a sequence's end, inside its pages:
+    never read into the result (both kernels), equal to the contiguous call."""
+    d = cuda_device
+    for Hq, page_size in ((8, 64), (32, 128)):
+        w = W.DecodeWorkload("fp8_paged_nan", 3, Hq, 2, 128, 700, 1, 700, 5555 + Hq)
+        q, k8, v8, ks, vs, _ = W.make_decode_fp8_inputs(w)
+        sl = torch.tensor([700, 1, 333], dtype=torch.int32)
+        for b in range(3):
+            n = int(sl[b])
+            k8[b, :, n:, :] = W.E4M3_NAN
+            v8[b, :, n:, :] = W.E4M3_NAN
+        kp, vp, bt = W.page_cache(k8, v8, page_size, seed=9)
+        args = (q.to(d), kp.to(d), vp.to(d), ks.to(d), vs.to(d), bt.to(d), sl.to(d))
+        out = gqa_lib.gqa_decode_fp8_paged(*args, scale=w.scale)
+        assert gqa_lib.gqa_get_device_status() == 0
+        o = out.double().cpu().numpy()
+        assert np.isfinite(o).all()
+        ref = oracle_fp8(oracle_mod, q, k8, v8, ks, vs, sl, w.scale)
+        assert_parity(o, ref, f"fp8 paged NaN tail G={Hq // 2}")
+        out_c = gqa_lib.gqa_decode_fp8(q.to(d), k8.to(d), v8.to(d), ks.to(d), vs.to(d), sl.to(d), scale=w.scale)
+        assert torch.equal(out, out_c)

@@ -77,10 +77,12 @@ def test_decode_step_graph_appends_and_decodes(gqa_lib, oracle_mod, cuda_device)
 def test_wide_group_decode_and_prefills_in_one_graph(gqa_lib, oracle_mod, cuda_device):
     """A wide-group decode (G = 32, the tcgen05 kernel with pairs cut across
     CTAs and merged in the launch), the same decode through the no-alloc entry
-    point, a causal prefill and a chunked prefill captured together; two
+    point and over FP8 pages, a causal prefill and a chunked prefill captured
+    together; two
     replays on fresh inputs both match the oracle (the merge counters a replay
-    leaves behind are the zeros the next one needs), and the no-alloc output
-    equals the other bit for bit."""
+    leaves behind are the zeros the next one needs), the no-alloc output
+    equals the other bit for bit, and the FP8-page output equals the
+    contiguous FP8 call on the same quantised cache."""
     dev = cuda_device
     # decode: ragged lengths spread over many CTAs, so pairs are cut
     dB, dHq, dHkv, dD, dLmax = 24, 32, 1, 128, 2048
@@ -91,6 +93,15 @@ def test_wide_group_decode_and_prefills_in_one_graph(gqa_lib, oracle_mod, cuda_d
     dsl = dl.to(dev)
     dout = torch.empty_like(dq)
     nout = torch.empty_like(dq)
+    # the same decode over FP8 pages (128-row pages of E4M3 bytes, unit scales)
+    page = 128
+    mp = dLmax // page
+    f_kp = torch.zeros(dB * mp, dHkv, page, dD, dtype=torch.uint8, device=dev)
+    f_vp = torch.zeros_like(f_kp)
+    f_bt = torch.randperm(dB * mp, generator=_gen(5210)).to(torch.int32).reshape(dB, mp).to(dev)
+    f_ks = torch.ones(dB, dHkv, dtype=torch.float32, device=dev)
+    f_vs = torch.ones_like(f_ks)
+    f_out = torch.empty_like(dq)
     # prefill (causal, G = 4) and a 100-token chunk after 284 cached ones
     pB, pHq, pHkv, pL, pD = 1, 8, 2, 384, 128
     pq = torch.empty(pB, pHq, pL, pD, dtype=torch.bfloat16, device=dev)
@@ -104,12 +115,14 @@ def test_wide_group_decode_and_prefills_in_one_graph(gqa_lib, oracle_mod, cuda_d
         t.zero_()
     gqa_lib.gqa_decode(dq, dk, dv, dsl, out=dout)
     gqa_lib.gqa_decode_noalloc(dq, dk, dv, dsl, nout)
+    gqa_lib.gqa_decode_fp8_paged(dq, f_kp, f_vp, f_ks, f_vs, f_bt, dsl, out=f_out)
     torch.cuda.synchronize()
 
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         gqa_lib.gqa_decode(dq, dk, dv, dsl, out=dout)
         gqa_lib.gqa_decode_noalloc(dq, dk, dv, dsl, nout)
+        gqa_lib.gqa_decode_fp8_paged(dq, f_kp, f_vp, f_ks, f_vs, f_bt, dsl, out=f_out)
         gqa_lib.gqa_prefill(pq, pk, pv, out=pout, causal=True)
         gqa_lib.gqa_prefill_chunk(cq, pk, pv, out=cout, causal=True)
 
@@ -119,11 +132,21 @@ def test_wide_group_decode_and_prefills_in_one_graph(gqa_lib, oracle_mod, cuda_d
         h_pq, h_pk, h_pv, h_cq = _bf16(pq.shape, g), _bf16(pk.shape, g), _bf16(pv.shape, g), _bf16(cq.shape, g)
         for d, h in ((dq, hq), (dk, hk), (dv, hv), (pq, h_pq), (pk, h_pk), (pv, h_pv), (cq, h_cq)):
             d.copy_(h)
+        k8, v8, ks8, vs8 = W.quantize_kv_fp8(hk, hv)
+        bt_h = f_bt.cpu()
+        for b in range(dB):
+            for i in range(mp):
+                f_kp[int(bt_h[b, i])].copy_(k8[b, :, i * page:(i + 1) * page].to(dev))
+                f_vp[int(bt_h[b, i])].copy_(v8[b, :, i * page:(i + 1) * page].to(dev))
+        f_ks.copy_(ks8)
+        f_vs.copy_(vs8)
         graph.replay()
         torch.cuda.synchronize()
         ref = oracle_mod.decode(W.bf16_bits(hq), W.bf16_bits(hk), W.bf16_bits(hv), dl.numpy(), dD ** -0.5)
         assert_parity(dout.double().cpu().numpy(), ref, f"decode replay {rep}")
         assert torch.equal(nout, dout)
+        f_ref = gqa_lib.gqa_decode_fp8(dq, k8.to(dev), v8.to(dev), f_ks, f_vs, dsl)
+        assert torch.equal(f_out, f_ref)
         ref = oracle_mod.prefill(W.bf16_bits(h_pq), W.bf16_bits(h_pk), W.bf16_bits(h_pv), causal=True)
         assert_parity(pout.double().cpu().numpy(), ref, f"prefill replay {rep}")
         ref = oracle_mod.prefill_chunk(W.bf16_bits(h_cq), W.bf16_bits(h_pk), W.bf16_bits(h_pv), causal=True)
